@@ -1,0 +1,245 @@
+"""Python binding of libcpa.so: chunked prefill attention with past for GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of libcpa.so; there is no fallback, and every call raises if the
+library has not been built.  torch supplies device memory and the current
+stream.  The entry points mirror include/cpa.h:
+
+    chunk_prefill_attn   one chunk of C rows against the KV cache
+    decode_step          the C = 1 case
+    kv_append            append the chunk (rotated K, V) to the cache
+    kv_snapshot_padded_append / kv_rollback_padded_append
+                         make a padded append to a sliding-window cache
+                         byte-identical to an unpadded one
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "decode_step",
+    "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
+    "attn_workspace_size", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+GLOBAL, SLIDING = 0, 1
+EBIT = dict(CAPACITY=1, PAST_GT_SPAN=2, NREAL_GT_C=4, SLIDING_N=8, SNAPSHOT=16, TIMEOUT=32)
+
+
+class CpaError(RuntimeError):
+    """A cpa_status other than CPA_OK."""
+
+    def __init__(self, status: int, text: str):
+        super().__init__(f"cpa status {status}: {text}")
+        self.status = status
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64), ("stride_s", ctypes.c_int64), ("len", ctypes.c_void_p),
+                ("cap", ctypes.c_int32), ("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("sink", ctypes.c_int32)]
+
+
+class _AttnArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+                ("C", ctypes.c_int), ("P", ctypes.c_int), ("scale", ctypes.c_float),
+                ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("cache", ctypes.POINTER(_Cache)),
+                ("mask", ctypes.c_void_p), ("past_len", ctypes.c_void_p), ("n_real", ctypes.c_void_p),
+                ("window", ctypes.c_int), ("causal", ctypes.c_int), ("sel_row", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("out_sel", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("err", ctypes.c_void_p)]
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libcpa.so")
+
+
+def load_library():
+    """Load libcpa.so (raises if it is missing: run build() first)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "chunked_prefill_attention_rope_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.cpa_chunk_prefill_attn.argtypes = [ctypes.POINTER(_AttnArgs), vp]
+    lib.cpa_decode_step.argtypes = [ctypes.POINTER(_AttnArgs), vp]
+    lib.cpa_attn_workspace_size.argtypes = [i32] * 6
+    lib.cpa_attn_workspace_size.restype = sz
+    lib.cpa_kv_append.argtypes = [ctypes.POINTER(_Cache), vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, sz, vp, vp]
+    lib.cpa_cache_scratch_size.argtypes = [ctypes.POINTER(_Cache), i32, i32, i32, i32]
+    lib.cpa_cache_scratch_size.restype = sz
+    lib.cpa_kv_snapshot_padded_append.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, vp, sz, vp, vp]
+    lib.cpa_kv_rollback_padded_append.argtypes = [ctypes.POINTER(_Cache), i32, i32, i32, i32, vp, sz, vp, vp]
+    lib.cpa_status_str.argtypes = [i32]
+    lib.cpa_status_str.restype = ctypes.c_char_p
+    lib.cpa_version.restype = ctypes.c_char_p
+    for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_kv_append",
+              "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append"):
+        getattr(lib, f).restype = i32
+    _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise CpaError(status, load_library().cpa_status_str(status).decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def new_error_word(device="cuda") -> torch.Tensor:
+    """A zeroed device int32 word for the library's CPA_EBIT_* flags."""
+    return torch.zeros(4, dtype=torch.int32, device=device)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+class KVCache:
+    """One layer's KV cache: k, v bf16 [B, Hkv, cap, D] (strided views allowed,
+    last dim contiguous), len int32 [B] on the device, and its kind."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, length: torch.Tensor, kind: int = GLOBAL,
+                 window: int = 0, sink: int = 0):
+        if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+            raise TypeError("cache k/v must be bf16")
+        if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 4 or k.stride(3) != 1:
+            raise ValueError("cache k/v: same [B, Hkv, cap, D] shape and strides, last dim contiguous")
+        _need(length, "len", torch.int32, (k.shape[0],))
+        self.k, self.v, self.len = k, v, length
+        self.kind, self.window, self.sink = kind, window, sink
+        self.B, self.Hkv, self.cap, self.D = k.shape
+
+    def struct(self) -> _Cache:
+        return _Cache(self.k.data_ptr(), self.v.data_ptr(), self.k.stride(0), self.k.stride(1),
+                      self.k.stride(2), self.len.data_ptr(), self.cap, self.kind, self.window, self.sink)
+
+
+def attn_workspace_size(B, Hq, Hkv, D, C, P) -> int:
+    return int(load_library().cpa_attn_workspace_size(B, Hq, Hkv, D, C, P))
+
+
+def cache_scratch_size(cache: KVCache, C: int) -> int:
+    s = cache.struct()
+    return int(load_library().cpa_cache_scratch_size(ctypes.byref(s), cache.B, cache.Hkv, cache.D, C))
+
+
+def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
+          window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
+          out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None):
+    lib = load_library()
+    B, Hq, C, D = q.shape
+    Hkv = k_new.shape[1]
+    _need(q, "q", torch.bfloat16)
+    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, C, D))
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, C, D))
+    _need(cos, "cos", torch.float32, (B, C, D))
+    _need(sin, "sin", torch.float32, (B, C, D))
+    if mask is not None:
+        _need(mask, "mask", torch.float32, (B, Hq, C, P + C))
+    for t, name in ((past_len, "past_len"), (n_real, "n_real"), (sel_row, "sel_row")):
+        if t is not None:
+            _need(t, name, torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, Hq, C, D))
+    if out_sel is None and want_sel:
+        out_sel = torch.empty((B, Hq * D), dtype=torch.float32, device=q.device)
+    need = lib.cpa_attn_workspace_size(B, Hq, Hkv, D, C, P)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if err is None:
+        err = new_error_word(q.device)
+    cs = cache.struct()
+    a = _AttnArgs(B, Hq, Hkv, D, C, P, float(scale), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                  cos.data_ptr(), sin.data_ptr(), ctypes.pointer(cs), _ptr(mask), _ptr(past_len),
+                  _ptr(n_real), int(window), 1 if causal else 0, _ptr(sel_row), out.data_ptr(),
+                  _ptr(out_sel), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                  err.data_ptr())
+    _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream)))
+    return out, out_sel
+
+
+def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
+    """Attention of one chunk (q [B,Hq,C,D], k_new/v_new [B,Hkv,C,D] bf16, cos/sin
+    [B,C,D] fp32) over cache slots [0, P) plus the chunk.  Returns (out, out_sel)."""
+    return _attn("cpa_chunk_prefill_attn", q, k_new, v_new, cos, sin, cache, P, **kw)
+
+
+def decode_step(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
+    """One-token decode (C = 1).  Returns (out, out_sel)."""
+    kw.setdefault("causal", False)
+    return _attn("cpa_decode_step", q, k_new, v_new, cos, sin, cache, P, **kw)
+
+
+def kv_append(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch=None, err=None, stream=None):
+    """Append rows [0, n_rows[b]) of the chunk (K rotated, V copied) to the cache."""
+    lib = load_library()
+    B, Hkv, C, D = k_new.shape
+    _need(k_new, "k_new", torch.bfloat16)
+    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, C, D))
+    _need(cos, "cos", torch.float32, (B, C, D))
+    _need(sin, "sin", torch.float32, (B, C, D))
+    _need(n_rows, "n_rows", torch.int32, (B,))
+    if err is None:
+        err = new_error_word(k_new.device)
+    cs = cache.struct()
+    if scratch is None and cache.kind == SLIDING:
+        scratch = torch.empty(cache_scratch_size(cache, C), dtype=torch.uint8, device=k_new.device)
+    _check(lib.cpa_kv_append(ctypes.byref(cs), k_new.data_ptr(), v_new.data_ptr(), cos.data_ptr(),
+                             sin.data_ptr(), n_rows.data_ptr(), B, Hkv, D, C, _ptr(scratch),
+                             0 if scratch is None else scratch.numel(), err.data_ptr(), _stream(stream)))
+    return err
+
+
+def kv_snapshot_padded_append(cache: KVCache, n_real, C: int, scratch, err=None, stream=None):
+    """Save the rows a padded append of C rows would over-evict (sliding caches)."""
+    lib = load_library()
+    _need(n_real, "n_real", torch.int32, (cache.B,))
+    if err is None:
+        err = new_error_word(n_real.device)
+    cs = cache.struct()
+    _check(lib.cpa_kv_snapshot_padded_append(ctypes.byref(cs), n_real.data_ptr(), cache.B, cache.Hkv,
+                                             cache.D, C, scratch.data_ptr(), scratch.numel(),
+                                             err.data_ptr(), _stream(stream)))
+    return err
+
+
+def kv_rollback_padded_append(cache: KVCache, C: int, scratch, err=None, stream=None):
+    """Drop the pad rows and reinsert the saved rows after a padded append."""
+    lib = load_library()
+    if err is None:
+        err = new_error_word(cache.len.device)
+    cs = cache.struct()
+    _check(lib.cpa_kv_rollback_padded_append(ctypes.byref(cs), cache.B, cache.Hkv, cache.D, C,
+                                             scratch.data_ptr(), scratch.numel(), err.data_ptr(),
+                                             _stream(stream)))
+    return err

@@ -1,0 +1,290 @@
+// C-ABI entry points (include/cpa.h): host-side validation, TMA descriptors,
+// split-KV policy and kernel launches.  Nothing here allocates device memory
+// or synchronises.
+#include <math.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace cpa;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 map {D, rows, heads, batch} with a {64, box_rows, 1, 1} box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int rows, int heads, int batch, int64_t s_row,
+              int64_t s_head, int64_t s_batch, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows > 0 ? rows : 1),
+                        static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row) * 2, static_cast<cuuint64_t>(s_head) * 2,
+                           static_cast<cuuint64_t>(s_batch) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+struct Geometry {
+  int G, R, nq, splits;
+};
+
+// Split-KV policy.  The host cannot see per-sequence lengths without a sync,
+// so the split count depends only on the shapes: grow splits while the grid is
+// under two waves, and for decode-like steps (one query tile per kv head) cap
+// a CTA at about 16 key tiles of the longest possible past.
+Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
+  Geometry g;
+  g.G = Hq / Hkv;
+  g.R = 128 / g.G;
+  g.nq = (C + g.R - 1) / g.R;
+  const int bn = attn_block_n(D);
+  const int max_tiles = (P + bn - 1) / bn + (C + bn - 1) / bn;
+  const long long ctas = static_cast<long long>(B) * Hkv * g.nq;
+  const int sms = num_sms();
+  int s = 1;
+  while (ctas * s < 2LL * sms && s * 2 <= max_tiles) s *= 2;
+  if (g.nq == 1 && max_tiles > 32) s = max(s, (max_tiles + 15) / 16);
+  g.splits = max(1, min(s, max(1, max_tiles)));
+  return g;
+}
+
+size_t workspace_bytes(const Geometry& g, int B, int Hq, int D, int C) {
+  if (g.splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * C;
+  const size_t o = static_cast<size_t>(g.splits) * rows * D * sizeof(float);
+  const size_t lse = static_cast<size_t>(g.splits) * rows * sizeof(float);
+  return ((o + 255) & ~size_t(255)) + lse;
+}
+
+bool valid_d(int D) { return D == 64 || D == 128 || D == 256; }
+
+cpa_status check_cache(const cpa_cache* c, int D) {
+  if (!c || !c->k || !c->v || !c->len) return CPA_ERR_NULL;
+  if (c->cap < 1 || c->stride_s < D || c->stride_h < 1 || c->stride_b < 1) return CPA_ERR_SHAPE;
+  if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->len)) return CPA_ERR_ALIGN;
+  if (c->stride_s % 8 || c->stride_h % 8 || c->stride_b % 8) return CPA_ERR_ALIGN;
+  if (c->kind != CPA_CACHE_GLOBAL && c->kind != CPA_CACHE_SLIDING) return CPA_ERR_SHAPE;
+  if (c->kind == CPA_CACHE_SLIDING) {
+    if (c->window < 1 || c->window > c->cap || c->sink < 0 || c->sink >= c->window) return CPA_ERR_SHAPE;
+  }
+  return CPA_OK;
+}
+
+CacheView view_of(const cpa_cache* c) {
+  CacheView v;
+  v.k = static_cast<uint16_t*>(c->k);
+  v.v = static_cast<uint16_t*>(c->v);
+  v.sb = c->stride_b;
+  v.sh = c->stride_h;
+  v.ss = c->stride_s;
+  v.len = c->len;
+  v.cap = c->cap;
+  v.window = c->kind == CPA_CACHE_SLIDING ? c->window : c->cap;
+  v.sink = c->kind == CPA_CACHE_SLIDING ? c->sink : 0;
+  return v;
+}
+
+cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
+  if (!a) return CPA_ERR_NULL;
+  if (!a->q || !a->k_new || !a->v_new || !a->cos || !a->sin || !a->out || !a->err) return CPA_ERR_NULL;
+  if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->C < 1 || a->P < 0) return CPA_ERR_SHAPE;
+  if (a->Hq % a->Hkv != 0 || a->Hq / a->Hkv > 128) return CPA_ERR_SHAPE;
+  if (!valid_d(a->D)) return CPA_ERR_UNSUPPORTED;
+  if (decode && a->C != 1) return CPA_ERR_SHAPE;
+  if (a->window < 0) return CPA_ERR_SHAPE;
+  const cpa_status cs = check_cache(a->cache, a->D);
+  if (cs != CPA_OK) return cs;
+  if (a->P > a->cache->cap) return CPA_ERR_SHAPE;
+  if (!a->mask) {
+    if (!a->past_len || !a->n_real) return CPA_ERR_NULL;
+    if (a->cache->kind == CPA_CACHE_SLIDING && a->cache->sink > 0) return CPA_ERR_UNSUPPORTED;
+  }
+  if (a->out_sel && !a->sel_row && !a->n_real) return CPA_ERR_NULL;
+  if (!aligned16(a->q) || !aligned16(a->k_new) || !aligned16(a->v_new) || !aligned16(a->cos) ||
+      !aligned16(a->sin) || !aligned16(a->out) || (a->out_sel && !aligned16(a->out_sel)) ||
+      (a->mask && !aligned16(a->mask)) || !aligned16(a->err))
+    return CPA_ERR_ALIGN;
+  if (static_cast<long long>(a->B) * a->Hq * a->C * a->D > (1LL << 40)) return CPA_ERR_SHAPE;
+
+  const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
+  const size_t need = workspace_bytes(g, a->B, a->Hq, a->D, a->C);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)))
+    return CPA_ERR_WORKSPACE;
+
+  const int bn = attn_block_n(a->D);
+  CUtensorMap maps[4];
+  const cpa_cache* c = a->cache;
+  const int64_t cs_ = static_cast<int64_t>(a->C) * a->D;
+  if (!make_map(&maps[0], c->k, a->D, a->P, a->Hkv, a->B, c->stride_s, c->stride_h, c->stride_b, bn) ||
+      !make_map(&maps[1], c->v, a->D, a->P, a->Hkv, a->B, c->stride_s, c->stride_h, c->stride_b, bn) ||
+      !make_map(&maps[2], a->k_new, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn) ||
+      !make_map(&maps[3], a->v_new, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn))
+    return CPA_ERR_CUDA;
+
+  AttnParams p{};
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.D = a->D;
+  p.C = a->C;
+  p.P = a->P;
+  p.G = g.G;
+  p.R = g.R;
+  p.nq = g.nq;
+  p.splits = g.splits;
+  const double scale = a->scale > 0.f ? static_cast<double>(a->scale) : 1.0 / sqrt(static_cast<double>(a->D));
+  p.sl2 = static_cast<float>(scale * 1.4426950408889634);
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.cos = a->cos;
+  p.sin = a->sin;
+  p.mask = a->mask;
+  p.past_len = a->past_len;
+  p.n_real = a->n_real;
+  p.sel_row = a->sel_row;
+  p.window = a->window;
+  p.causal = a->causal ? 1 : 0;
+  p.out = static_cast<uint16_t*>(a->out);
+  p.out_sel = a->out_sel;
+  p.err = a->err;
+  if (g.splits > 1) {
+    const size_t rows = static_cast<size_t>(a->B) * a->Hq * a->C;
+    const size_t o = static_cast<size_t>(g.splits) * rows * a->D * sizeof(float);
+    p.part_o = static_cast<float*>(a->workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + ((o + 255) & ~size_t(255)));
+  }
+  return launch_attn(maps, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+}
+
+cpa_status chunk_check(const void* k_new, const void* v_new, const float* cos, const float* sin,
+                       const int32_t* n_rows, int B, int Hkv, int D, int C, int32_t* err) {
+  if (!k_new || !v_new || !cos || !sin || !n_rows || !err) return CPA_ERR_NULL;
+  if (B < 1 || Hkv < 1 || C < 1) return CPA_ERR_SHAPE;
+  if (!valid_d(D)) return CPA_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cos) || !aligned16(sin) || !aligned16(err))
+    return CPA_ERR_ALIGN;
+  return CPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cpa_status cpa_chunk_prefill_attn(const cpa_attn_args* args, cpa_stream stream) {
+  return attn_impl(args, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream) {
+  return attn_impl(args, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || C < 1 || P < 0 || Hq % Hkv || Hq / Hkv > 128 || !valid_d(D)) return 0;
+  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, D, C);
+}
+
+size_t cpa_cache_scratch_size(const cpa_cache* cache, int B, int Hkv, int D, int C) {
+  if (!cache || cache->kind != CPA_CACHE_SLIDING || B < 1 || Hkv < 1 || C < 1 || !valid_d(D)) return 0;
+  return sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
+}
+
+cpa_status cpa_kv_append(const cpa_cache* cache, const void* k_new, const void* v_new, const float* cos,
+                         const float* sin, const int32_t* n_rows, int B, int Hkv, int D, int C, void* scratch,
+                         size_t scratch_bytes, int32_t* err, cpa_stream stream) {
+  cpa_status st = chunk_check(k_new, v_new, cos, sin, n_rows, B, Hkv, D, C, err);
+  if (st != CPA_OK) return st;
+  if ((st = check_cache(cache, D)) != CPA_OK) return st;
+  const CacheView cv = view_of(cache);
+  ChunkView x{static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), cos, sin, n_rows};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cache->kind == CPA_CACHE_GLOBAL) {
+    e = launch_global_append(cv, x, B, Hkv, D, C, err, s);
+  } else {
+    const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
+    if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
+    e = launch_sliding_append(cv, x, B, Hkv, D, C, static_cast<uint8_t*>(scratch), err, s);
+  }
+  return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+}
+
+cpa_status cpa_kv_snapshot_padded_append(const cpa_cache* cache, const int32_t* n_real, int B, int Hkv, int D,
+                                         int C, void* scratch, size_t scratch_bytes, int32_t* err,
+                                         cpa_stream stream) {
+  if (!n_real || !err) return CPA_ERR_NULL;
+  if (B < 1 || Hkv < 1 || C < 1) return CPA_ERR_SHAPE;
+  if (!valid_d(D)) return CPA_ERR_UNSUPPORTED;
+  cpa_status st = check_cache(cache, D);
+  if (st != CPA_OK) return st;
+  if (cache->kind != CPA_CACHE_SLIDING) return CPA_ERR_UNSUPPORTED;
+  if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
+  const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
+  if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
+  return launch_snapshot(view_of(cache), n_real, B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CPA_OK
+             : CPA_ERR_CUDA;
+}
+
+cpa_status cpa_kv_rollback_padded_append(const cpa_cache* cache, int B, int Hkv, int D, int C, void* scratch,
+                                         size_t scratch_bytes, int32_t* err, cpa_stream stream) {
+  if (!err) return CPA_ERR_NULL;
+  if (B < 1 || Hkv < 1 || C < 1) return CPA_ERR_SHAPE;
+  if (!valid_d(D)) return CPA_ERR_UNSUPPORTED;
+  cpa_status st = check_cache(cache, D);
+  if (st != CPA_OK) return st;
+  if (cache->kind != CPA_CACHE_SLIDING) return CPA_ERR_UNSUPPORTED;
+  if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
+  const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
+  if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
+  return launch_rollback(view_of(cache), B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CPA_OK
+             : CPA_ERR_CUDA;
+}
+
+const char* cpa_status_str(cpa_status s) {
+  switch (s) {
+    case CPA_OK: return "ok";
+    case CPA_ERR_NULL: return "a required pointer is NULL";
+    case CPA_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case CPA_ERR_ALIGN: return "a pointer or stride is misaligned";
+    case CPA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CPA_ERR_WINDOW_TOO_SMALL: return "sliding window too small for a padded append (W <= C + S)";
+    case CPA_ERR_WORKSPACE: return "workspace or scratch too small";
+    case CPA_ERR_CUDA: return "CUDA launch error";
+  }
+  return "unknown status";
+}
+
+const char* cpa_version(void) { return "cpa 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,535 @@
+// Chunk-prefill attention with past on tcgen05 tensor cores (sm_103a).
+//
+// What it computes ("functiongemma: chunk prefill-with-past graph", Change):
+// a chunk of C query rows, rotated with per-position cos/sin tables, attends
+// over P cached key slots followed by the C chunk rows (chunk keys rotated with
+// the same tables) under an additive mask; softmax-weighted values per row.
+//
+// Work decomposition.  One CTA owns 128 packed query rows of one (sequence b,
+// kv head): R = floor(128 / G) chunk rows for each of the G query heads that
+// share the kv head (row r <-> head g = r / R, chunk row i = i0 + r % R), so K
+// and V tiles are loaded once for the whole GQA group.  Key tiles of BN keys
+// are visited chunk tiles first, then past tiles; tiles that the implicit mask
+// leaves fully masked for every row of the CTA are never visited.  A CTA may
+// take only a slice of its key tiles (split-KV); the slices are merged by
+// combine_kernel.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: K and V tiles into a 2-stage shared-memory ring.
+//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM S buffers,
+//               O += P V into the TMEM O accumulator; owns the TMEM allocation.
+//   warps 2..5  softmax warpgroup: thread = TMEM lane = packed query row.
+//               Rotates Q into shared memory at the start, rotates each raw
+//               chunk-K tile in place, applies the mask, keeps the running
+//               max / sum in fp32 (log2 domain, rescaling O only when the max
+//               grows by more than 2^8), writes P as bf16, and finally scales
+//               O by 1/l and stores it.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cpa {
+
+constexpr int kBM = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaskedLog2 = -1e30f * kLog2e;  // the masked score, in log2 units
+constexpr float kEmptyRow = -1e28f;              // running max below this: no visible key
+
+struct __align__(8) AttnBars {
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], k_rot[kStages];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full, pv_done, q_ready, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, int BN>
+struct AttnSmem {
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKBytes = BN * D * 2;
+  static constexpr int kVBytes = BN * D * 2;
+  static constexpr int kPBytes = kBM * BN * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kV = kK + kStages * kKBytes;
+  static constexpr int kP = kV + kStages * kVBytes;
+  static constexpr int kBars = kP + kPBytes;
+  static constexpr int kTotal = kBars + static_cast<int>(sizeof(AttnBars));
+  static constexpr int kAlloc = kTotal + 1024;  // room to align the base to 1024
+  static constexpr int kSCol = 0;               // S buffers at columns [0, 2*BN)
+  static constexpr int kOCol = 2 * BN;          // O at columns [2*BN, 2*BN + D)
+  static_assert(2 * BN + D <= 512, "TMEM columns");
+  static_assert(kAlloc <= 232448, "shared memory");
+};
+
+// Tile bookkeeping shared by every role of the CTA.
+struct TilePlan {
+  int L, n;         // clamped past length and real rows of this sequence
+  int c0, nc;       // chunk tiles [c0, c0 + nc)
+  int p0, np;       // past tiles [p0, p0 + np)
+  int t_begin, t_end;
+};
+
+template <int BN>
+__device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int qt, int split) {
+  TilePlan t;
+  int L = p.past_len ? p.past_len[b] : p.P;
+  int n = p.n_real ? p.n_real[b] : p.C;
+  t.L = min(max(L, 0), p.P);
+  t.n = min(max(n, 0), p.C);
+  if (p.mask) {
+    t.c0 = 0;
+    t.nc = (p.C + BN - 1) / BN;
+    t.p0 = 0;
+    t.np = (p.P + BN - 1) / BN;
+  } else {
+    const int W = p.window;
+    const int i_min = qt * p.R;
+    const int i_max = min(i_min + p.R, p.C) - 1;
+    const int t_lo = W > 0 ? max(0, i_min - W + 1) : 0;
+    const int t_hi = p.causal ? min(t.n, i_max + 1) : (W > 0 ? min(t.n, i_max + W) : t.n);
+    const int j_lo = W > 0 ? max(0, t.L + i_min - W + 1) : 0;
+    const int j_hi = t.L;
+    t.c0 = t_lo / BN;
+    t.nc = t_hi > t_lo ? (t_hi + BN - 1) / BN - t.c0 : 0;
+    t.p0 = j_lo / BN;
+    t.np = j_hi > j_lo ? (j_hi + BN - 1) / BN - t.p0 : 0;
+  }
+  const int nt = t.nc + t.np;
+  t.t_begin = static_cast<int>((static_cast<long long>(nt) * split) / p.splits);
+  t.t_end = static_cast<int>((static_cast<long long>(nt) * (split + 1)) / p.splits);
+  return t;
+}
+
+template <int D, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
+                const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
+                const AttnParams p) {
+  using SM = AttnSmem<D, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  AttnBars* bars = reinterpret_cast<AttnBars*>(smem + SM::kBars);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int qt = blockIdx.x / p.splits;
+  const int split = blockIdx.x % p.splits;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const TilePlan tp = plan_tiles<BN>(p, b, qt, split);
+  const int my_nt = tp.t_end - tp.t_begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_rot[s], 128);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_empty[s], 128);
+    }
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+    if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P) && kvh == 0 && blockIdx.x == 0)
+      set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
+    if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C) && kvh == 0 && blockIdx.x == 0)
+      set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  uint8_t* sQ = smem + SM::kQ;
+  uint8_t* sK = smem + SM::kK;
+  uint8_t* sV = smem + SM::kV;
+  uint8_t* sP = smem + SM::kP;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && my_nt > 0) {
+      prefetch_tensormap(&map_kc);
+      prefetch_tensormap(&map_vc);
+      prefetch_tensormap(&map_kn);
+      prefetch_tensormap(&map_vn);
+      int issued = 0;
+      for (int q = 0; q < my_nt; ++q) {
+        const int st = q % kStages;
+        if (!mbar_wait(&bars->kv_empty[st], ((q / kStages) + 1) & 1, abort)) break;
+        const int j = tp.t_begin + q;
+        const bool chunk = j < tp.nc;
+        const int base = chunk ? (tp.c0 + j) * BN : (tp.p0 + j - tp.nc) * BN;
+        const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
+        const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
+        mbar_arrive_expect_tx(&bars->k_full[st], SM::kKBytes);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(sK + st * SM::kKBytes + blk * BN * 128, mk, &bars->k_full[st], blk * 64, base, kvh, b);
+        mbar_arrive_expect_tx(&bars->v_full[st], SM::kVBytes);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(sV + st * SM::kVBytes + blk * BN * 128, mv, &bars->v_full[st], blk * 64, base, kvh, b);
+        issued = q + 1;
+      }
+      // Before leaving, make sure no copy is still landing in shared memory.
+      for (int q = max(0, issued - kStages); q < issued; ++q) {
+        const int st = q % kStages;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars->v_full[st], (q / kStages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_try_wait(&bars->k_full[st], (q / kStages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kBM, BN, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, true);
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t p_addr = smem_u32(sP);
+      bool ok = my_nt > 0 ? mbar_wait(&bars->q_ready, 0, abort) : true;
+      auto issue_pv = [&](int q) -> bool {
+        const int st = q % kStages;
+        if (!mbar_wait(&bars->p_full, q & 1, abort)) return false;
+        if (!mbar_wait(&bars->v_full[st], (q / kStages) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + st * SM::kVBytes);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(p_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, BN * 128, 1024);
+          mma_bf16_ss(tmem + SM::kOCol, a, bd, idesc_pv, (q > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->pv_done);
+        mma_commit(&bars->kv_empty[st]);
+        return true;
+      };
+      for (int q = 0; ok && q < my_nt; ++q) {
+        const int st = q % kStages;
+        const int sb = q & 1;
+        const int j = tp.t_begin + q;
+        ok = mbar_wait(j < tp.nc ? &bars->k_rot[st] : &bars->k_full[st], (q / kStages) & 1, abort);
+        if (!ok) break;
+        ok = mbar_wait(&bars->s_empty[sb], ((q >> 1) + 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * SM::kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(q_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_addr + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+          mma_bf16_ss(tmem + SM::kSCol + sb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[sb]);
+        if (q > 0) ok = issue_pv(q - 1);
+      }
+      if (ok && my_nt > 0) issue_pv(my_nt - 1);
+      // Every MMA issued above has finished once this barrier flips.
+      mma_commit(&bars->mma_done);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bars->mma_done, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int tid = threadIdx.x - 64;               // 0..127
+    const int row = 32 * (warp & 3) + lane;         // TMEM lane owned by this thread
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int g = row / p.R;
+    const int i = qt * p.R + row % p.R;
+    const bool valid = g < p.G && i < p.C;
+    const int h = kvh * p.G + (valid ? g : 0);
+
+    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.
+    for (int item = tid; item < kBM * (D / 16); item += 128) {
+      const int r = item / (D / 16);
+      const int kc = item % (D / 16);
+      const int rg = r / p.R;
+      const int ri = qt * p.R + r % p.R;
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (rg < p.G && ri < p.C) {
+        const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + rg) * p.C + ri) * D;
+        lo = *reinterpret_cast<const uint4*>(p.q + rowoff + kc * 8);
+        hi = *reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc * 8);
+        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
+        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
+        rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+      }
+      const int kh = kc + D / 16;
+      *reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8)) = lo;
+      *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi;
+    }
+    fence_async_smem();
+    mbar_arrive(&bars->q_ready);
+
+    // Visible key intervals of this row (implicit mask).
+    const int W = p.window;
+    const int past_lo = W > 0 ? max(0, tp.L + i - W + 1) : 0;
+    const int ch_lo = W > 0 ? max(0, i - W + 1) : 0;
+    const int ch_hi = p.causal ? min(tp.n, i + 1) : (W > 0 ? min(tp.n, i + W) : tp.n);
+    const float* mrow = (p.mask && valid)
+                            ? p.mask + ((static_cast<size_t>(b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C)
+                            : nullptr;
+
+    float m_run = kMaskedLog2, l_run = 0.f;
+    bool ok = true;
+    for (int q = 0; q < my_nt; ++q) {
+      const int st = q % kStages;
+      const int sb = q & 1;
+      const int j = tp.t_begin + q;
+      const bool chunk = j < tp.nc;
+      const int base = chunk ? (tp.c0 + j) * BN : (tp.p0 + j - tp.nc) * BN;
+      if (chunk) {
+        // rotate the raw chunk-K tile in place
+        if (!(ok = warp_all(mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort)))) break;
+        uint8_t* kt = sK + st * SM::kKBytes;
+        for (int item = tid; item < BN * (D / 16); item += 128) {
+          const int r = item / (D / 16);
+          const int kc = item % (D / 16);
+          const int t = base + r;
+          if (t >= p.C) continue;
+          const int kh = kc + D / 16;
+          uint4* plo = reinterpret_cast<uint4*>(kt + (kc / 8) * (BN * 128) + sw128(r, kc % 8));
+          uint4* phi = reinterpret_cast<uint4*>(kt + (kh / 8) * (BN * 128) + sw128(r, kh % 8));
+          uint4 lo = *plo, hi = *phi;
+          const float* cr = p.cos + (static_cast<size_t>(b) * p.C + t) * D;
+          const float* sr = p.sin + (static_cast<size_t>(b) * p.C + t) * D;
+          rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+          *plo = lo;
+          *phi = hi;
+        }
+        fence_async_smem();
+        mbar_arrive(&bars->k_rot[st]);
+      }
+      if (!(ok = warp_all(mbar_wait(&bars->s_full[sb], (q >> 1) & 1, abort)))) break;
+      tc_fence_after();
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r32[32];
+        tmem_ld32(tmem + lane_base + SM::kSCol + sb * BN + 32 * c, r32);
+        tmem_ld_wait(r32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r32[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_empty[sb]);
+
+      // scale + mask, in log2 units
+      if (mrow) {
+        const bool pastt = !chunk;
+        const int lim = pastt ? p.P : p.C;
+        const float* mp = mrow + (pastt ? base : p.P + base);
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const float mv = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+          x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(mv, kLog2e));
+        }
+      } else {
+        const int lo = (chunk ? ch_lo : past_lo) - base;
+        const int hi = valid ? ((chunk ? ch_hi : tp.L) - base) : -1;
+#pragma unroll
+        for (int e = 0; e < BN; ++e) x[e] = (e >= lo && e < hi) ? __fmul_rn(x[e], p.sl2) : kMaskedLog2;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int e = 1; e < BN; ++e) mt = fmaxf(mt, x[e]);
+      float m_use, factor = 1.f;
+      bool rescale = false;
+      if (q == 0) {
+        m_use = mt;
+      } else {
+        const float m_new = fmaxf(m_run, mt);
+        rescale = (m_new - m_run) > 8.f;
+        m_use = rescale ? m_new : m_run;
+        if (rescale) factor = fast_exp2(m_run - m_new);
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        x[e] = fast_exp2(__fsub_rn(x[e], m_use));
+        sum += x[e];
+      }
+      l_run = (q == 0) ? sum : __fmaf_rn(l_run, factor, sum);
+      m_run = m_use;
+
+      // P buffer and O are free once the previous P V has finished.
+      if (q > 0) {
+        if (!(ok = warp_all(mbar_wait(&bars->pv_done, (q - 1) & 1, abort)))) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o32[32];
+            const uint32_t ta = tmem + lane_base + SM::kOCol + 32 * c;
+            tmem_ld32(ta, o32);
+            tmem_ld_wait(o32);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o32[e] = __float_as_uint(__uint_as_float(o32[e]) * factor);
+            tmem_st32(ta, o32);
+          }
+          tmem_st_wait();
+        }
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < BN / 8; ++c8) {
+        uint4 w;
+        w.x = pack_bf16x2(x[8 * c8 + 0], x[8 * c8 + 1]);
+        w.y = pack_bf16x2(x[8 * c8 + 2], x[8 * c8 + 3]);
+        w.z = pack_bf16x2(x[8 * c8 + 4], x[8 * c8 + 5]);
+        w.w = pack_bf16x2(x[8 * c8 + 6], x[8 * c8 + 7]);
+        *reinterpret_cast<uint4*>(sP + (c8 / 8) * (kBM * 128) + sw128(row, c8 % 8)) = w;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+
+    // ---------------------------------------------------------- epilogue
+    if (ok && my_nt > 0) ok = warp_all(mbar_wait(&bars->pv_done, (my_nt - 1) & 1, abort));
+    tc_fence_after();
+    const bool empty = !(my_nt > 0 && ok && m_run > kEmptyRow);
+    const float inv_l = empty ? 0.f : 1.f / l_run;
+    const int sel = valid ? (p.sel_row ? p.sel_row[b] : tp.n - 1) : -1;
+    const size_t orow = ((static_cast<size_t>(b) * p.Hq + h) * p.C + i);
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o32[32];
+      if (my_nt > 0) {
+        tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c, o32);
+        tmem_ld_wait(o32);
+      }
+      float o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : __uint_as_float(o32[e]) * inv_l;
+      if (!valid) continue;
+      if (p.part_o) {
+        float* dst = p.part_o + ((static_cast<size_t>(split) * p.B * p.Hq * p.C) + orow) * D + 32 * c;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+      } else {
+        uint16_t* dst = p.out + orow * D + 32 * c;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = pack_bf16x2(o[e + 0], o[e + 1]);
+          w.y = pack_bf16x2(o[e + 2], o[e + 3]);
+          w.z = pack_bf16x2(o[e + 4], o[e + 5]);
+          w.w = pack_bf16x2(o[e + 6], o[e + 7]);
+          *reinterpret_cast<uint4*>(dst + e) = w;
+        }
+        if (p.out_sel && i == sel) {
+          float* sd = p.out_sel + (static_cast<size_t>(b) * p.Hq + h) * D + 32 * c;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(sd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        }
+      }
+    }
+    if (valid && p.part_lse) {
+      p.part_lse[static_cast<size_t>(split) * p.B * p.Hq * p.C + orow] =
+          empty ? -INFINITY : m_run + __log2f(l_run);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && bars->abort) set_err(p.err, CPA_EBIT_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge split-KV partials in fixed split order: one warp per output row.
+__global__ void combine_kernel(const AttnParams p) {
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const int rows = p.B * p.Hq * p.C;
+  if (warp_global >= rows) return;
+  const size_t row = warp_global;
+  const int i = static_cast<int>(row % p.C);
+  const int bh = static_cast<int>(row / p.C);
+  const int b = bh / p.Hq;
+  const int h = bh % p.Hq;
+  const size_t stride = static_cast<size_t>(rows);
+  float lmax = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) lmax = fmaxf(lmax, p.part_lse[s * stride + row]);
+  const int D = p.D;
+  const int per = D / 32;  // 2, 4 or 8 values per lane
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (lmax != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const float ls = p.part_lse[s * stride + row];
+      if (ls == -INFINITY) continue;
+      const float w = fast_exp2(ls - lmax);
+      wsum += w;
+      const float* src = p.part_o + (s * stride + row) * D + lane * per;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e < per) acc[e] = __fmaf_rn(w, src[e], acc[e]);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  int n = p.n_real ? min(max(p.n_real[b], 0), p.C) : p.C;
+  const int sel = p.sel_row ? p.sel_row[b] : n - 1;
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    if (e < per) {
+      const float o0 = acc[e] * inv, o1 = acc[e + 1] * inv;
+      *reinterpret_cast<uint32_t*>(p.out + row * D + lane * per + e) = pack_bf16x2(o0, o1);
+      if (p.out_sel && i == sel) {
+        float* sd = p.out_sel + (static_cast<size_t>(b) * p.Hq + h) * D + lane * per + e;
+        sd[0] = o0;
+        sd[1] = o1;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int D, int BN>
+static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+  using SM = AttnSmem<D, BN>;
+  auto kern = attn_kernel<D, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.nq * p.splits, p.Hkv, p.B);
+  kern<<<grid, kThreads, SM::kAlloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int rows = p.B * p.Hq * p.C;
+  const int threads = 256;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  combine_kernel<<<blocks, threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int attn_block_n(int D) { return D == 256 ? 64 : 128; }
+
+cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 64: return launch_attn_t<64, 128>(maps, p, stream);
+    case 128: return launch_attn_t<128, 128>(maps, p, stream);
+    case 256: return launch_attn_t<256, 64>(maps, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace cpa

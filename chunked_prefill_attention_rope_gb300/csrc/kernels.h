@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cpa {
+
+struct AttnParams {
+  int B, Hq, Hkv, D, C, P, G, R, nq, splits;
+  float sl2;  // softmax scale * log2(e)
+  const uint16_t* q;
+  const float* cos;
+  const float* sin;
+  const float* mask;
+  const int32_t* past_len;
+  const int32_t* n_real;
+  const int32_t* sel_row;
+  int window, causal;
+  uint16_t* out;
+  float* out_sel;
+  float* part_o;    // split-KV partials [splits][B][Hq][C][D] or null
+  float* part_lse;  // [splits][B][Hq][C]
+  int32_t* err;
+};
+
+int attn_block_n(int D);
+// maps: cache K, cache V (dims {D, P, Hkv, B}), chunk K, chunk V (dims {D, C, Hkv, B}),
+// all bf16, box {64, block_n, 1, 1}, 128-byte swizzle.
+cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
+
+struct CacheView {
+  uint16_t* k;
+  uint16_t* v;
+  int64_t sb, sh, ss;  // strides in elements
+  int32_t* len;
+  int cap, window, sink;
+};
+
+struct ChunkView {
+  const uint16_t* k;  // [B, Hkv, C, D]
+  const uint16_t* v;
+  const float* cos;   // [B, C, D]
+  const float* sin;
+  const int32_t* n_rows;
+};
+
+// Scratch layout of a sliding cache (byte offsets from the scratch base).
+struct SlidingScratch {
+  size_t hdr_append, hdr_snap, hdr_roll, saved_k, saved_v, stage_k, stage_v, total;
+};
+SlidingScratch sliding_scratch_layout(int B, int Hkv, int D, int C, int W);
+
+cudaError_t launch_global_append(const CacheView& c, const ChunkView& x, int B, int Hkv, int D, int C,
+                                 int32_t* err, cudaStream_t s);
+cudaError_t launch_sliding_append(const CacheView& c, const ChunkView& x, int B, int Hkv, int D, int C,
+                                  uint8_t* scratch, int32_t* err, cudaStream_t s);
+cudaError_t launch_snapshot(const CacheView& c, const int32_t* n_real, int B, int Hkv, int D, int C,
+                            uint8_t* scratch, int32_t* err, cudaStream_t s);
+cudaError_t launch_rollback(const CacheView& c, int B, int Hkv, int D, int C, uint8_t* scratch,
+                            int32_t* err, cudaStream_t s);
+
+}  // namespace cpa

@@ -1,0 +1,80 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C-ABI
+binding and the fp64 oracle on the same seeded bytes, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+from synth import bf16_bits
+
+MAX_ABS = 1e-2     # attention output tolerance, max |gpu - oracle|
+REL_L2 = 3e-3      # attention output tolerance, ||gpu - oracle|| / ||oracle||
+ARGMAX_GAP = 2e-2  # oracle top-1 minus top-2 gap above which the argmax must match exactly
+
+
+def lib():
+    import chunked_prefill_attention_rope_gb300 as cpa
+    from chunked_prefill_attention_rope_gb300.build import build
+    build()
+    return cpa
+
+
+def compare(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str = ""):
+    """max-abs and rel-L2 of a bf16 GPU tensor against an fp64 oracle array."""
+    g = gpu_bf16.detach().float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    d = np.abs(g - ref)
+    max_abs = float(d.max()) if d.size else 0.0
+    den = float(np.sqrt(np.sum(ref ** 2)))
+    rel = float(np.sqrt(np.sum(d ** 2)) / den) if den > 0 else max_abs
+    return max_abs, rel
+
+
+def assert_close(gpu_bf16, ref, what=""):
+    max_abs, rel = compare(gpu_bf16, ref, what)
+    assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={max_abs:.3e} rel_l2={rel:.3e}"
+    return max_abs, rel
+
+
+def check_argmax(gpu_sel: torch.Tensor, ref_sel: np.ndarray, what=""):
+    """Selected-row argmax: exact when the oracle's top-2 gap exceeds ARGMAX_GAP;
+    otherwise the GPU's pick must be one of the near-tied oracle maxima."""
+    g = gpu_sel.detach().float().cpu().numpy()
+    r32 = ref_sel.astype(np.float32)
+    for b in range(r32.shape[0]):
+        gi = int(O.select_argmax(g[b]))
+        ri = int(O.select_argmax(r32[b]))
+        top2 = np.sort(r32[b])[-2:]
+        gap = float(top2[1] - top2[0])
+        if gap > ARGMAX_GAP:
+            assert gi == ri, f"{what}: argmax {gi} != oracle {ri} (gap {gap:.3e})"
+        else:
+            assert r32[b, ri] - r32[b, gi] <= ARGMAX_GAP, f"{what}: argmax {gi} not near-tied with {ri}"
+
+
+def cache_bytes(t: torch.Tensor) -> np.ndarray:
+    return bf16_bits(t)
+
+
+def oracle_attn(q, k_new, v_new, cos, sin, ck, cv, P, past_len, n_real, window=0, causal=1,
+                mask=None, sel_row=None):
+    """Run the oracle on host copies of torch tensors."""
+    f = lambda t: None if t is None else t.detach().cpu()
+    L = f(past_len).numpy() if past_len is not None else None
+    n = f(n_real).numpy() if n_real is not None else None
+    m = None if mask is None else f(mask).numpy()
+    s = None if sel_row is None else f(sel_row).numpy()
+    return O.chunk_prefill_attn(bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new), f(cos).numpy(),
+                                f(sin).numpy(), bf16_bits(ck), bf16_bits(cv), P, L, n,
+                                window=window, causal=causal, mask=m, sel_row=s)
+
+
+def explicit_masks(past_len, n_real, C, P, Hq, window, causal):
+    """[B, Hq, C, P+C] fp32 additive masks built by the oracle's mask function."""
+    B = len(past_len)
+    out = np.zeros((B, Hq, C, P + C), dtype=np.float32)
+    for b in range(B):
+        out[b] = O.explicit_mask(int(past_len[b]), int(n_real[b]), C, P, window, causal)[None]
+    return torch.from_numpy(out)

@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry point
+include/cpa.h declares, and rejects bad arguments on the host (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_prefill_attention_rope_gb300.build import build
+    build()
+    import chunked_prefill_attention_rope_gb300 as cpa
+    return cpa, cpa.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "cpa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    _, so = lib
+    names = declared_functions()
+    assert len(names) == 9, names
+    for name in names:
+        assert hasattr(so, name), name
+
+
+def test_status_strings_and_version(lib):
+    _, so = lib
+    assert so.cpa_status_str(0) == b"ok"
+    assert b"W <= C + S" in so.cpa_status_str(5)
+    assert so.cpa_version().startswith(b"cpa")
+
+
+def test_workspace_sizes(lib):
+    cpa, so = lib
+    # bad shapes -> 0; a decode-like step needs split-KV partials
+    assert so.cpa_attn_workspace_size(1, 3, 2, 128, 1, 10) == 0
+    assert so.cpa_attn_workspace_size(1, 4, 1, 96, 1, 10) == 0
+    assert so.cpa_attn_workspace_size(64, 32, 8, 128, 1, 32768) > 0
+
+
+def _args(cpa, **kw):
+    a = cpa._AttnArgs()
+    a.B, a.Hq, a.Hkv, a.D, a.C, a.P = 1, 4, 1, 64, 16, 48
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_host_validation_returns_status_without_launch(lib):
+    cpa, so = lib
+    call = lambda a: so.cpa_chunk_prefill_attn(ctypes.byref(a), None)
+    assert call(_args(cpa)) == 1                         # NULL pointers
+    fake = 0x10000                                       # never dereferenced: validation fails first
+    cache = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 0, 0, 0)
+    full = dict(q=fake, k_new=fake, v_new=fake, cos=fake, sin=fake, out=fake, err=fake,
+                cache=ctypes.pointer(cache), past_len=fake, n_real=fake)
+    assert call(_args(cpa, D=96, **full)) == 4           # unsupported head dim
+    assert call(_args(cpa, Hq=3, Hkv=2, **full)) == 2    # Hq not a multiple of Hkv
+    assert call(_args(cpa, P=65, **full)) == 2           # span beyond capacity
+    assert call(_args(cpa, **dict(full, q=fake + 2))) == 3  # misaligned
+    bad = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 68, fake, 64, 0, 0, 0)
+    assert call(_args(cpa, **dict(full, cache=ctypes.pointer(bad)))) == 3  # stride not a multiple of 8
+    assert so.cpa_decode_step(ctypes.byref(_args(cpa, **full)), None) == 2  # decode needs C == 1
+    sl = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 1, 32, 4)
+    assert call(_args(cpa, **dict(full, cache=ctypes.pointer(sl)))) == 4   # implicit mask with sinks
+
+
+def test_sliding_guards(lib):
+    cpa, so = lib
+    fake = 0x10000
+    sl = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 1, 24, 8)
+    # W = 24 <= C + S = 16 + 8
+    assert so.cpa_kv_snapshot_padded_append(ctypes.byref(sl), fake, 1, 1, 64, 16, fake, 1 << 30, fake, None) == 5
+    assert so.cpa_kv_rollback_padded_append(ctypes.byref(sl), 1, 1, 64, 16, fake, 1 << 30, fake, None) == 5
+    glob = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 0, 0, 0)
+    assert so.cpa_kv_snapshot_padded_append(ctypes.byref(glob), fake, 1, 1, 64, 16, fake, 1 << 30, fake, None) == 4
+    ok = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 1, 40, 0)
+    need = so.cpa_cache_scratch_size(ctypes.byref(ok), 1, 1, 64, 16)
+    assert need > 0
+    assert so.cpa_kv_snapshot_padded_append(ctypes.byref(ok), fake, 1, 1, 64, 16, fake, need - 1, fake, None) == 6
+    assert so.cpa_cache_scratch_size(ctypes.byref(glob), 1, 1, 64, 16) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import chunked_prefill_attention_rope_gb300 as cpa
+    monkeypatch.setattr(cpa, "_LIB", None)
+    monkeypatch.setattr(cpa, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        cpa.load_library()

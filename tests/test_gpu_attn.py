@@ -1,0 +1,201 @@
+"""GPU parity of chunk-prefill attention and decode against the fp64 oracle.
+
+Outputs within max-abs 1e-2 and rel-L2 3e-3 of the oracle; explicit and
+implicit masks bitwise identical; two runs bitwise identical; selected-row
+argmax exact unless the oracle's top-2 gap is within tolerance.
+Sources: "functiongemma: chunk prefill-with-past graph gemma_prefill_with_past"
+(Change: RoPE tables, per-head additive mask over past + C keys, one-hot select;
+Validation: 800 cached + 52-token chunk, C = 64, select row 51) and
+"[quanization] Enable prefill-decode modeling" (Mask/cache layout).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import WORKLOADS, Workload, make_chunk_inputs, make_cache, normal_bf16, rope_tables
+from harness import lib, assert_close, check_argmax, oracle_attn, explicit_masks
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_gpu(cpa, inp, ck, cv, P, window=0, causal=True, mask=None, sel_row=None, want_sel=True,
+            kind=0, wsize=0, sink=0):
+    d = lambda t: None if t is None else t.to(DEV)
+    cache = cpa.KVCache(d(ck), d(cv), d(inp["past_len"]).clone(), kind, wsize, sink)
+    err = cpa.new_error_word()
+    out, sel = cpa.chunk_prefill_attn(d(inp["q"]), d(inp["k"]), d(inp["v"]), d(inp["cos"]), d(inp["sin"]),
+                                      cache, P, past_len=d(inp["past_len"]), n_real=d(inp["n_real"]),
+                                      window=window, causal=causal, mask=d(mask), sel_row=d(sel_row),
+                                      want_sel=want_sel, err=err)
+    torch.cuda.synchronize()
+    return out, sel, err
+
+
+def small(name, B, Hq, Hkv, D, C, P, L, n, window=0, causal=1, seed=0):
+    return Workload(name, B=B, Hq=Hq, Hkv=Hkv, D=D, C=C, P=P, cap=P + C, past=L, n_real=n,
+                    window=window, causal=causal, seed=seed)
+
+
+CASES = [
+    WORKLOADS["tiny"],
+    small("s_d128_g4", 2, 8, 2, 128, 40, 300, ("uniform", 0, 300), ("uniform", 1, 40)),
+    small("s_d64_g1", 3, 2, 2, 64, 130, 257, ("uniform", 0, 257), ("uniform", 0, 130)),
+    small("s_d256_g8", 1, 8, 1, 256, 128, 512, ("fixed", 512), ("fixed", 127), window=512),
+    small("s_win_small", 2, 4, 1, 128, 64, 200, ("uniform", 50, 200), ("uniform", 30, 64), window=37),
+    small("s_noncausal_win", 2, 4, 2, 64, 33, 100, ("uniform", 0, 100), ("uniform", 1, 33), window=9, causal=0),
+    small("s_noncausal", 1, 4, 4, 128, 17, 140, ("fixed", 139), ("fixed", 17), causal=0),
+    small("s_g16", 1, 16, 1, 128, 20, 64, ("fixed", 64), ("fixed", 20)),
+    small("s_empty_past", 2, 4, 1, 128, 96, 0, ("fixed", 0), ("uniform", 0, 96)),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_attention_matches_oracle_and_explicit_is_bitwise_implicit(w):
+    cpa = lib()
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    out_i, sel_i, err = run_gpu(cpa, inp, ck, cv, w.P, w.window, bool(w.causal))
+    assert int(err[0]) == 0
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                               inp["past_len"], inp["n_real"], w.window, w.causal,
+                               sel_row=(inp["n_real"] - 1).clamp(min=0))
+    assert_close(out_i, ref, w.name)
+    if (inp["n_real"] > 0).all():
+        assert_close(sel_i.view(w.B, w.Hq, w.D).to(torch.bfloat16), ref_sel.reshape(w.B, w.Hq, w.D), w.name + "/sel")
+        check_argmax(sel_i, ref_sel, w.name)
+    mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, w.window, w.causal)
+    out_e, sel_e, err = run_gpu(cpa, inp, ck, cv, w.P, mask=mask)
+    assert int(err[0]) == 0
+    assert torch.equal(out_e.view(torch.int16), out_i.view(torch.int16)), "explicit != implicit"
+    out_2, _, _ = run_gpu(cpa, inp, ck, cv, w.P, w.window, bool(w.causal))
+    assert torch.equal(out_2.view(torch.int16), out_i.view(torch.int16)), "not deterministic"
+
+
+def test_implicit_ignores_dead_cache_rows():
+    """Slots at or past past_len never influence the implicit path."""
+    cpa = lib()
+    w = small("dead_rows", 2, 8, 2, 128, 32, 400, ("uniform", 10, 300), ("fixed", 32))
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    out1, _, _ = run_gpu(cpa, inp, ck, cv, w.P)
+    ck2, cv2 = ck.clone(), cv.clone()
+    for b in range(w.B):
+        L = int(inp["past_len"][b])
+        ck2[b, :, L:] = normal_bf16(ck2[b, :, L:].shape, 1, f"dead/k{b}")
+        cv2[b, :, L:] = normal_bf16(cv2[b, :, L:].shape, 1, f"dead/v{b}")
+    out2, _, _ = run_gpu(cpa, inp, ck2, cv2, w.P)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_page1_shape_eighteen_layers_explicit_masks():
+    """800 cached positions + a 52-token chunk padded to 64, select row 51, 18 layers
+    alternating a 512-position window (base 1e4) and global attention (base 1e6),
+    one explicit [1, 4, 64, 864] mask and one cos/sin pair per layer type."""
+    cpa = lib()
+    w = WORKLOADS["page1"]
+    L = w.past_lens(); n = w.n_reals()
+    masks, tabs = {}, {}
+    for kind, W, base in (("sliding", 512, 1e4), ("global", 0, 1e6)):
+        masks[kind] = explicit_masks(L.numpy(), n.numpy(), w.C, w.P, w.Hq, W, 1)
+        tabs[kind] = rope_tables(L.numpy()[:, None] + np.arange(w.C)[None, :], w.D, base)
+    # per-type sharing: 1 (tokens) + 2 bases x 2 tables + 18 x (K, V) + 2 masks + 1 select = 44
+    assert 1 + 2 * len(tabs) + 2 * w.layers + len(masks) + 1 == 44
+    sel = torch.full((w.B,), 51, dtype=torch.int32)
+    for layer in range(w.layers):
+        kind = "sliding" if layer % 2 == 0 else "global"
+        inp = make_chunk_inputs(w, layer=layer)
+        inp["cos"], inp["sin"] = tabs[kind]
+        ck, cv = make_cache(w, layer=layer)
+        out, sel_out, err = run_gpu(cpa, inp, ck, cv, w.P, mask=masks[kind], sel_row=sel)
+        assert int(err[0]) == 0
+        ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                                   L, n, mask=masks[kind], sel_row=sel)
+        assert_close(out, ref, f"page1/L{layer}")
+        check_argmax(sel_out, ref_sel, f"page1/L{layer}")
+        # the implicit description of the same mask gives the same bits
+        out_i, _, _ = run_gpu(cpa, inp, ck, cv, w.P, window=512 if kind == "sliding" else 0, sel_row=sel)
+        assert torch.equal(out_i.view(torch.int16), out.view(torch.int16)), f"page1/L{layer} implicit"
+
+
+def sample_check(cpa, w, pairs, device_gen=False):
+    """Run the full workload on the GPU, check sampled (b, kv-head) groups on the oracle."""
+    dev = DEV if device_gen else "cpu"
+    inp = make_chunk_inputs(w, device=dev)
+    ck, cv = make_cache(w, device=dev)
+    d = lambda t: t.to(DEV)
+    cache = cpa.KVCache(d(ck), d(cv), d(inp["past_len"]).clone())
+    err = cpa.new_error_word()
+    out, sel = cpa.chunk_prefill_attn(d(inp["q"]), d(inp["k"]), d(inp["v"]), d(inp["cos"]), d(inp["sin"]),
+                                      cache, w.P, past_len=d(inp["past_len"]), n_real=d(inp["n_real"]),
+                                      causal=bool(w.causal), want_sel=True, err=err)
+    torch.cuda.synchronize()
+    assert int(err[0]) == 0
+    G = w.Hq // w.Hkv
+    u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    for b, kvh in pairs:
+        hs = slice(kvh * G, (kvh + 1) * G)
+        L = int(inp["past_len"][b])
+        ref, _ = O.chunk_prefill_attn(
+            u16(inp["q"][b:b + 1, hs]), u16(inp["k"][b:b + 1, kvh:kvh + 1]),
+            u16(inp["v"][b:b + 1, kvh:kvh + 1]), inp["cos"][b:b + 1].cpu().numpy(),
+            inp["sin"][b:b + 1].cpu().numpy(), u16(ck[b:b + 1, kvh:kvh + 1, :L]),
+            u16(cv[b:b + 1, kvh:kvh + 1, :L]), L, [L], [int(inp["n_real"][b])], causal=w.causal)
+        assert_close(out[b:b + 1, hs], ref, f"{w.name}/b{b}/kvh{kvh}")
+    return out
+
+
+def test_packed_batch_full_size_sampled():
+    cpa = lib()
+    w = WORKLOADS["packed_batch"]
+    L = w.past_lens()
+    order = np.argsort(L.numpy())
+    pairs = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
+    sample_check(cpa, w, pairs)
+
+
+def test_long_context_full_size_sampled():
+    cpa = lib()
+    sample_check(cpa, WORKLOADS["long_ctx"], [(0, 0), (3, 7)], device_gen=True)
+
+
+def test_decode_full_size_sampled():
+    cpa = lib()
+    w = WORKLOADS["decode"]
+    inp = make_chunk_inputs(w, device=DEV)
+    ck, cv = make_cache(w, device=DEV)
+    cache = cpa.KVCache(ck, cv, inp["past_len"].clone())
+    err = cpa.new_error_word()
+    out, _ = cpa.decode_step(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], cache, w.P,
+                             past_len=inp["past_len"], n_real=inp["n_real"], err=err)
+    torch.cuda.synchronize()
+    assert int(err[0]) == 0
+    G = w.Hq // w.Hkv
+    Ls = inp["past_len"].cpu().numpy()
+    picks = [int(np.argmin(Ls)), int(np.argmax(Ls)), 17]
+    u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    for b in picks:
+        for kvh in (0, 5):
+            L = int(Ls[b])
+            hs = slice(kvh * G, (kvh + 1) * G)
+            ref = O.decode_step(u16(inp["q"][b:b + 1, hs]), u16(inp["k"][b:b + 1, kvh:kvh + 1]),
+                                u16(inp["v"][b:b + 1, kvh:kvh + 1]), inp["cos"][b:b + 1].cpu().numpy(),
+                                inp["sin"][b:b + 1].cpu().numpy(), u16(ck[b:b + 1, kvh:kvh + 1, :L]),
+                                u16(cv[b:b + 1, kvh:kvh + 1, :L]), L, [L])
+            assert_close(out[b:b + 1, hs], ref, f"decode/b{b}/kvh{kvh}")
+
+
+def test_out_of_range_lengths_are_flagged_and_clamped():
+    cpa = lib()
+    w = small("bad_len", 2, 4, 1, 64, 8, 32, ("fixed", 10), ("fixed", 8))
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    inp["past_len"] = torch.tensor([40, 5], dtype=torch.int32)   # 40 > P = 32
+    inp["n_real"] = torch.tensor([8, 9], dtype=torch.int32)      # 9 > C = 8
+    out, _, err = run_gpu(cpa, inp, ck, cv, w.P, want_sel=False)
+    e = int(err[0])
+    assert e & cpa.EBIT["PAST_GT_SPAN"] and e & cpa.EBIT["NREAL_GT_C"]
+    ref, _ = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                         torch.tensor([32, 5]), torch.tensor([8, 8]))
+    assert_close(out, ref, "clamped")
