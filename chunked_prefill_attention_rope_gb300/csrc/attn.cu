@@ -64,11 +64,22 @@ struct AttnSmem {
 };
 
 // Tile bookkeeping shared by every role of the CTA.
+//
+// Key tiles live in one index space known on the host: tiles [0, Tc) are chunk
+// tiles (chunk rows [t*BN, t*BN + BN)), tiles [Tc, Tc + Tp) are past tiles
+// (slots [(t-Tc)*BN, ...)).  Split s owns the fixed index range
+// [s*T/S, (s+1)*T/S) and visits the live tiles inside it.  The implicit mask
+// makes the live set two intervals; with an explicit mask every tile is live.
+// Because the ranges do not depend on the mask, the explicit and implicit
+// descriptions of one mask split the keys identically; the extra tiles the
+// explicit path visits are fully masked and contribute exactly zero.
 struct TilePlan {
-  int L, n;         // clamped past length and real rows of this sequence
-  int c0, nc;       // chunk tiles [c0, c0 + nc)
-  int p0, np;       // past tiles [p0, p0 + np)
-  int t_begin, t_end;
+  int L, n;       // clamped past length and real rows of this sequence
+  int Tc;         // chunk tiles in the index space
+  int cb, ce;     // chunk tiles visited: index range [cb, ce)
+  int pb, pe;     // past tiles visited: index range [pb, pe)
+  __device__ __forceinline__ int count() const { return (ce - cb) + (pe - pb); }
+  __device__ __forceinline__ int index(int q) const { return q < ce - cb ? cb + q : pb + (q - (ce - cb)); }
 };
 
 template <int BN>
@@ -78,12 +89,10 @@ __device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int q
   int n = p.n_real ? p.n_real[b] : p.C;
   t.L = min(max(L, 0), p.P);
   t.n = min(max(n, 0), p.C);
-  if (p.mask) {
-    t.c0 = 0;
-    t.nc = (p.C + BN - 1) / BN;
-    t.p0 = 0;
-    t.np = (p.P + BN - 1) / BN;
-  } else {
+  t.Tc = (p.C + BN - 1) / BN;
+  const int Tp = (p.P + BN - 1) / BN;
+  int c0 = 0, c1 = t.Tc, q0 = 0, q1 = Tp;
+  if (!p.mask) {
     const int W = p.window;
     const int i_min = qt * p.R;
     const int i_max = min(i_min + p.R, p.C) - 1;
@@ -91,14 +100,18 @@ __device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int q
     const int t_hi = p.causal ? min(t.n, i_max + 1) : (W > 0 ? min(t.n, i_max + W) : t.n);
     const int j_lo = W > 0 ? max(0, t.L + i_min - W + 1) : 0;
     const int j_hi = t.L;
-    t.c0 = t_lo / BN;
-    t.nc = t_hi > t_lo ? (t_hi + BN - 1) / BN - t.c0 : 0;
-    t.p0 = j_lo / BN;
-    t.np = j_hi > j_lo ? (j_hi + BN - 1) / BN - t.p0 : 0;
+    c0 = t_lo / BN;
+    c1 = t_hi > t_lo ? (t_hi + BN - 1) / BN : c0;
+    q0 = j_lo / BN;
+    q1 = j_hi > j_lo ? (j_hi + BN - 1) / BN : q0;
   }
-  const int nt = t.nc + t.np;
-  t.t_begin = static_cast<int>((static_cast<long long>(nt) * split) / p.splits);
-  t.t_end = static_cast<int>((static_cast<long long>(nt) * (split + 1)) / p.splits);
+  const long long T = t.Tc + Tp;
+  const int r0 = static_cast<int>(T * split / p.splits);
+  const int r1 = static_cast<int>(T * (split + 1) / p.splits);
+  t.cb = max(c0, r0);
+  t.ce = max(t.cb, min(c1, r1));
+  t.pb = max(t.Tc + q0, r0);
+  t.pe = max(t.pb, min(t.Tc + q1, r1));
   return t;
 }
 
@@ -121,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
 
   const TilePlan tp = plan_tiles<BN>(p, b, qt, split);
-  const int my_nt = tp.t_end - tp.t_begin;
+  const int my_nt = tp.count();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -169,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < my_nt; ++q) {
         const int st = q % kStages;
         if (!mbar_wait(&bars->kv_empty[st], ((q / kStages) + 1) & 1, abort)) break;
-        const int j = tp.t_begin + q;
-        const bool chunk = j < tp.nc;
-        const int base = chunk ? (tp.c0 + j) * BN : (tp.p0 + j - tp.nc) * BN;
+        const int j = tp.index(q);
+        const bool chunk = j < tp.Tc;
+        const int base = (chunk ? j : j - tp.Tc) * BN;
         const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
         const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
         mbar_arrive_expect_tx(&bars->k_full[st], SM::kKBytes);
@@ -219,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; ok && q < my_nt; ++q) {
         const int st = q % kStages;
         const int sb = q & 1;
-        const int j = tp.t_begin + q;
-        ok = mbar_wait(j < tp.nc ? &bars->k_rot[st] : &bars->k_full[st], (q / kStages) & 1, abort);
+        const bool chunk = tp.index(q) < tp.Tc;
+        ok = mbar_wait(chunk ? &bars->k_rot[st] : &bars->k_full[st], (q / kStages) & 1, abort);
         if (!ok) break;
         ok = mbar_wait(&bars->s_empty[sb], ((q >> 1) + 1) & 1, abort);
         if (!ok) break;
@@ -288,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < my_nt; ++q) {
       const int st = q % kStages;
       const int sb = q & 1;
-      const int j = tp.t_begin + q;
-      const bool chunk = j < tp.nc;
-      const int base = chunk ? (tp.c0 + j) * BN : (tp.p0 + j - tp.nc) * BN;
+      const int j = tp.index(q);
+      const bool chunk = j < tp.Tc;
+      const int base = (chunk ? j : j - tp.Tc) * BN;
       if (chunk) {
         // rotate the raw chunk-K tile in place
         if (!(ok = warp_all(mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort)))) break;
