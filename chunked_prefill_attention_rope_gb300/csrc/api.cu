@@ -60,7 +60,8 @@ struct Geometry {
 // Split-KV policy.  The host cannot see per-sequence lengths without a sync,
 // so the split count depends only on the shapes: grow splits while the grid is
 // under two waves, and for decode-like steps (one query tile per kv head) cap
-// a CTA at about 16 key tiles of the longest possible past.
+// a CTA at about 16 key tiles of the longest possible past.  Each split owns a
+// fixed range of the key-tile index space (see tiles.cuh).
 Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   Geometry g;
   g.G = Hq / Hkv;
@@ -68,7 +69,8 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   g.nq = (C + g.R - 1) / g.R;
   const int bn = attn_block_n(D);
   const int max_tiles = (P + bn - 1) / bn + (C + bn - 1) / bn;
-  const long long ctas = static_cast<long long>(B) * Hkv * g.nq;
+  const int per_kv = attn_uses_pair(D, g.nq) ? (g.nq + 1) / 2 : g.nq;
+  const long long ctas = static_cast<long long>(B) * Hkv * per_kv;
   const int sms = num_sms();
   int s = 1;
   while (ctas * s < 2LL * sms && s * 2 <= max_tiles) s *= 2;

@@ -24,17 +24,13 @@
 //               max / sum in fp32 (log2 domain, rescaling O only when the max
 //               grows by more than 2^8), writes P as bf16, and finally scales
 //               O by 1/l and stores it.
-#include "common.cuh"
-#include "kernels.h"
+#include "tiles.cuh"
 
 namespace cpa {
 
 constexpr int kBM = 128;
 constexpr int kStages = 2;
 constexpr int kThreads = 192;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaskedLog2 = -1e30f * kLog2e;  // the masked score, in log2 units
-constexpr float kEmptyRow = -1e28f;              // running max below this: no visible key
 
 struct __align__(8) AttnBars {
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], k_rot[kStages];
@@ -63,58 +59,6 @@ struct AttnSmem {
   static_assert(kAlloc <= 232448, "shared memory");
 };
 
-// Tile bookkeeping shared by every role of the CTA.
-//
-// Key tiles live in one index space known on the host: tiles [0, Tc) are chunk
-// tiles (chunk rows [t*BN, t*BN + BN)), tiles [Tc, Tc + Tp) are past tiles
-// (slots [(t-Tc)*BN, ...)).  Split s owns the fixed index range
-// [s*T/S, (s+1)*T/S) and visits the live tiles inside it.  The implicit mask
-// makes the live set two intervals; with an explicit mask every tile is live.
-// Because the ranges do not depend on the mask, the explicit and implicit
-// descriptions of one mask split the keys identically; the extra tiles the
-// explicit path visits are fully masked and contribute exactly zero.
-struct TilePlan {
-  int L, n;       // clamped past length and real rows of this sequence
-  int Tc;         // chunk tiles in the index space
-  int cb, ce;     // chunk tiles visited: index range [cb, ce)
-  int pb, pe;     // past tiles visited: index range [pb, pe)
-  __device__ __forceinline__ int count() const { return (ce - cb) + (pe - pb); }
-  __device__ __forceinline__ int index(int q) const { return q < ce - cb ? cb + q : pb + (q - (ce - cb)); }
-};
-
-template <int BN>
-__device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int qt, int split) {
-  TilePlan t;
-  int L = p.past_len ? p.past_len[b] : p.P;
-  int n = p.n_real ? p.n_real[b] : p.C;
-  t.L = min(max(L, 0), p.P);
-  t.n = min(max(n, 0), p.C);
-  t.Tc = (p.C + BN - 1) / BN;
-  const int Tp = (p.P + BN - 1) / BN;
-  int c0 = 0, c1 = t.Tc, q0 = 0, q1 = Tp;
-  if (!p.mask) {
-    const int W = p.window;
-    const int i_min = qt * p.R;
-    const int i_max = min(i_min + p.R, p.C) - 1;
-    const int t_lo = W > 0 ? max(0, i_min - W + 1) : 0;
-    const int t_hi = p.causal ? min(t.n, i_max + 1) : (W > 0 ? min(t.n, i_max + W) : t.n);
-    const int j_lo = W > 0 ? max(0, t.L + i_min - W + 1) : 0;
-    const int j_hi = t.L;
-    c0 = t_lo / BN;
-    c1 = t_hi > t_lo ? (t_hi + BN - 1) / BN : c0;
-    q0 = j_lo / BN;
-    q1 = j_hi > j_lo ? (j_hi + BN - 1) / BN : q0;
-  }
-  const long long T = t.Tc + Tp;
-  const int r0 = static_cast<int>(T * split / p.splits);
-  const int r1 = static_cast<int>(T * (split + 1) / p.splits);
-  t.cb = max(c0, r0);
-  t.ce = max(t.cb, min(c1, r1));
-  t.pb = max(t.Tc + q0, r0);
-  t.pe = max(t.pb, min(t.Tc + q1, r1));
-  return t;
-}
-
 template <int D, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
@@ -133,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
 
-  const TilePlan tp = plan_tiles<BN>(p, b, qt, split);
+  const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
   const int my_nt = tp.count();
 
   if (threadIdx.x == 0) {
@@ -521,12 +465,18 @@ template <int D, int BN>
 static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   using SM = AttnSmem<D, BN>;
   auto kern = attn_kernel<D, BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
-  if (e != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
   kern<<<grid, kThreads, SM::kAlloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
   const int rows = p.B * p.Hq * p.C;
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
@@ -537,12 +487,19 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
 int attn_block_n(int D) { return D == 256 ? 64 : 128; }
 
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  switch (p.D) {
-    case 64: return launch_attn_t<64, 128>(maps, p, stream);
-    case 128: return launch_attn_t<128, 128>(maps, p, stream);
-    case 256: return launch_attn_t<256, 64>(maps, p, stream);
-    default: return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (attn_uses_pair(p.D, p.nq)) {
+    e = launch_attn_pair(maps, p, stream);
+  } else {
+    switch (p.D) {
+      case 64: e = launch_attn_t<64, 128>(maps, p, stream); break;
+      case 128: e = launch_attn_t<128, 128>(maps, p, stream); break;
+      case 256: e = launch_attn_t<256, 64>(maps, p, stream); break;
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (e != cudaSuccess || p.splits == 1) return e;
+  return launch_combine(p, stream);
 }
 
 }  // namespace cpa

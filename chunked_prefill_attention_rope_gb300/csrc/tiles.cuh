@@ -1,0 +1,79 @@
+// Key-tile bookkeeping shared by the attention kernels.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaskedLog2 = -1e30f * kLog2e;  // the masked score, in log2 units
+constexpr float kEmptyRow = -1e28f;              // running max below this: no visible key yet
+
+// Key tiles live in one index space known on the host: tiles [0, Tc) are chunk
+// tiles (chunk rows [t*BN, t*BN + BN)), tiles [Tc, Tc + Tp) are past tiles
+// (slots [(t-Tc)*BN, ...)).  Split s owns the fixed index range
+// [s*T/S, (s+1)*T/S) and visits the live tiles inside it.  The implicit mask
+// makes the live set two intervals; with an explicit mask every tile is live.
+// Because the ranges do not depend on the mask, the explicit and implicit
+// descriptions of one mask split the keys identically; the extra tiles the
+// explicit path visits are fully masked and contribute exactly zero.
+struct TilePlan {
+  int L, n;       // clamped past length and real rows of this sequence
+  int Tc;         // chunk tiles in the index space
+  int cb, ce;     // chunk tiles visited: index range [cb, ce)
+  int pb, pe;     // past tiles visited: index range [pb, pe)
+  __device__ __forceinline__ int count() const { return (ce - cb) + (pe - pb); }
+  __device__ __forceinline__ int index(int q) const { return q < ce - cb ? cb + q : pb + (q - (ce - cb)); }
+};
+
+// Live key tiles for query rows [i_min, i_max] of sequence b, restricted to split `split`.
+template <int BN>
+__device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int i_min, int i_max, int split) {
+  TilePlan t;
+  int L = p.past_len ? p.past_len[b] : p.P;
+  int n = p.n_real ? p.n_real[b] : p.C;
+  t.L = min(max(L, 0), p.P);
+  t.n = min(max(n, 0), p.C);
+  t.Tc = (p.C + BN - 1) / BN;
+  const int Tp = (p.P + BN - 1) / BN;
+  int c0 = 0, c1 = t.Tc, q0 = 0, q1 = Tp;
+  if (!p.mask) {
+    const int W = p.window;
+    const int t_lo = W > 0 ? max(0, i_min - W + 1) : 0;
+    const int t_hi = p.causal ? min(t.n, i_max + 1) : (W > 0 ? min(t.n, i_max + W) : t.n);
+    const int j_lo = W > 0 ? max(0, t.L + i_min - W + 1) : 0;
+    const int j_hi = t.L;
+    c0 = t_lo / BN;
+    c1 = t_hi > t_lo ? (t_hi + BN - 1) / BN : c0;
+    q0 = j_lo / BN;
+    q1 = j_hi > j_lo ? (j_hi + BN - 1) / BN : q0;
+  }
+  const long long T = t.Tc + Tp;
+  const int r0 = static_cast<int>(T * split / p.splits);
+  const int r1 = static_cast<int>(T * (split + 1) / p.splits);
+  t.cb = max(c0, r0);
+  t.ce = max(t.cb, min(c1, r1));
+  t.pb = max(t.Tc + q0, r0);
+  t.pe = max(t.pb, min(t.Tc + q1, r1));
+  return t;
+}
+
+// Visible key interval of query row i, relative to a tile's first key
+// (implicit mask): keys e with lo <= e < hi are visible.
+struct RowSpan {
+  int past_lo, ch_lo, ch_hi, L;
+  __device__ __forceinline__ void init(const AttnParams& p, const TilePlan& tp, int i, bool valid) {
+    const int W = p.window;
+    L = valid ? tp.L : 0;
+    past_lo = W > 0 ? max(0, tp.L + i - W + 1) : 0;
+    ch_lo = W > 0 ? max(0, i - W + 1) : 0;
+    ch_hi = !valid ? 0 : (p.causal ? min(tp.n, i + 1) : (W > 0 ? min(tp.n, i + W) : tp.n));
+  }
+  __device__ __forceinline__ void tile(bool chunk, int base, int& lo, int& hi) const {
+    lo = (chunk ? ch_lo : past_lo) - base;
+    hi = (chunk ? ch_hi : L) - base;
+  }
+};
+
+}  // namespace cpa
