@@ -21,7 +21,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "decode_step",
+    "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
+    "decode_step",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
     "attn_workspace_size", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
 ]
@@ -77,6 +78,7 @@ def load_library():
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.cpa_chunk_prefill_attn.argtypes = [ctypes.POINTER(_AttnArgs), vp]
     lib.cpa_decode_step.argtypes = [ctypes.POINTER(_AttnArgs), vp]
+    lib.cpa_chunk_prefill_attn_noalloc.argtypes = [ctypes.POINTER(_AttnArgs), vp]
     lib.cpa_attn_workspace_size.argtypes = [i32] * 6
     lib.cpa_attn_workspace_size.restype = sz
     lib.cpa_kv_append.argtypes = [ctypes.POINTER(_Cache), vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, sz, vp, vp]
@@ -87,7 +89,7 @@ def load_library():
     lib.cpa_status_str.argtypes = [i32]
     lib.cpa_status_str.restype = ctypes.c_char_p
     lib.cpa_version.restype = ctypes.c_char_p
-    for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_kv_append",
+    for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_chunk_prefill_attn_noalloc", "cpa_kv_append",
               "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append"):
         getattr(lib, f).restype = i32
     _LIB = lib
@@ -154,7 +156,8 @@ def cache_scratch_size(cache: KVCache, C: int) -> int:
 
 def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
           window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
-          out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None):
+          out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None,
+          alloc_workspace: bool = True):
     lib = load_library()
     B, Hq, C, D = q.shape
     Hkv = k_new.shape[1]
@@ -174,7 +177,7 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
     if out_sel is None and want_sel:
         out_sel = torch.empty((B, Hq * D), dtype=torch.float32, device=q.device)
     need = lib.cpa_attn_workspace_size(B, Hq, Hkv, D, C, P)
-    if workspace is None and need > 0:
+    if workspace is None and need > 0 and alloc_workspace:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if err is None:
         err = new_error_word(q.device)
@@ -192,6 +195,16 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
     """Attention of one chunk (q [B,Hq,C,D], k_new/v_new [B,Hkv,C,D] bf16, cos/sin
     [B,C,D] fp32) over cache slots [0, P) plus the chunk.  Returns (out, out_sel)."""
     return _attn("cpa_chunk_prefill_attn", q, k_new, v_new, cos, sin, cache, P, **kw)
+
+
+def chunk_prefill_attn_noalloc(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
+    """chunk_prefill_attn without a caller workspace: for callers that cannot
+    allocate device memory (graph capture, statically planned runtimes,
+    framework plugins).  Split-KV partials use the library's fixed 16 MiB
+    array; sizes needing more raise CpaError (CPA_ERR_WORKSPACE)."""
+    kw["workspace"] = None
+    return _attn("cpa_chunk_prefill_attn_noalloc", q, k_new, v_new, cos, sin, cache, P,
+                 alloc_workspace=False, **kw)
 
 
 def decode_step(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):

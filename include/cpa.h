@@ -168,6 +168,26 @@ cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream);
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P);
 
 /*
+ * cpa_chunk_prefill_attn for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this exists for callers with no way to obtain a
+ * workspace -- code running while a CUDA graph is captured, runtimes whose
+ * device memory is planned once from static shapes, and plugins inside a host
+ * framework that owns the allocator.  Arguments and results are those of
+ * cpa_chunk_prefill_attn; args->workspace and args->workspace_bytes are
+ * ignored.  Split-KV partials go to one 16 MiB array compiled into the library
+ * (held on every GPU that loads the library until the process exits); the
+ * call itself allocates nothing.
+ *   - Returns CPA_ERR_WORKSPACE, launching nothing, when the sizes need more
+ *     than 16 MiB (cpa_attn_workspace_size(...) > 16 MiB).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array, and no byte of it needs to start at zero
+ *     (each call writes every partial it reads).  Calls whose kernels overlap
+ *     on the GPU (different streams without ordering) race on the array.
+ */
+cpa_status cpa_chunk_prefill_attn_noalloc(const cpa_attn_args* args, cpa_stream stream);
+
+/*
  * Append rows [0, n_rows[b]) of the chunk to the cache ([P2, Runtime
  * behavior]: the runtime writes the step's K/V into the external cache;
  * [P1, Change]: K/V extended by the chunk).  K rows are rotated with cos/sin
