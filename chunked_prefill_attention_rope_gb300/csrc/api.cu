@@ -142,7 +142,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)))
     return CPA_ERR_WORKSPACE;
 
-  const int bn = attn_block_n(a->D);
+  const int bn = attn_uses_decode(a->D, a->C, g.G) ? 64 : attn_block_n(a->D);
   CUtensorMap maps[4];
   const cpa_cache* c = a->cache;
   const int64_t cs_ = static_cast<int64_t>(a->C) * a->D;

@@ -488,7 +488,9 @@ int attn_block_n(int D) { return D == 256 ? 64 : 128; }
 
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   cudaError_t e;
-  if (attn_uses_pair(p.D, p.nq)) {
+  if (attn_uses_decode(p.D, p.C, p.G)) {
+    e = launch_attn_decode(maps, p, stream);
+  } else if (attn_uses_pair(p.D, p.nq)) {
     e = launch_attn_pair(maps, p, stream);
   } else {
     switch (p.D) {

@@ -29,6 +29,9 @@ int attn_block_n(int D);
 // True when the two-query-tile kernel (256 packed rows per CTA) serves these sizes.
 inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >= 2; }
 cudaError_t launch_attn_pair(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
+// True when the warp-MMA decode kernel (64-key tiles, G <= 16 rows) serves these sizes.
+inline bool attn_uses_decode(int D, int C, int G) { return C == 1 && (D == 64 || D == 128) && G <= 16; }
+cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 // maps: cache K, cache V (dims {D, P, Hkv, B}), chunk K, chunk V (dims {D, C, Hkv, B}),
 // all bf16, box {64, block_n, 1, 1}, 128-byte swizzle.
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);

@@ -48,6 +48,10 @@ CASES = [
     small("s_noncausal", 1, 4, 4, 128, 17, 140, ("fixed", 139), ("fixed", 17), causal=0),
     small("s_g16", 1, 16, 1, 128, 20, 64, ("fixed", 64), ("fixed", 20)),
     small("s_empty_past", 2, 4, 1, 128, 96, 0, ("fixed", 0), ("uniform", 0, 96)),
+    small("d_decode", 3, 8, 2, 128, 1, 700, ("uniform", 1, 700), ("fixed", 1), causal=0),
+    small("d_decode_win", 2, 8, 2, 64, 1, 900, ("uniform", 300, 900), ("fixed", 1), window=100, causal=0),
+    small("d_decode_g16", 2, 16, 1, 128, 1, 257, ("uniform", 0, 257), ("fixed", 1), causal=0),
+    small("d_decode_g32", 1, 32, 1, 128, 1, 300, ("fixed", 299), ("fixed", 1), causal=0),
 ]
 
 
