@@ -29,16 +29,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D bf16 map {D, rows, heads, batch} with a {64, box_rows, 1, 1} box, 128-byte swizzle.
+// 4-D bf16 map {D, rows, heads, batch} with a {64, box_rows, box_heads, 1} box, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int D, int rows, int heads, int batch, int64_t s_row,
-              int64_t s_head, int64_t s_batch, int box_rows) {
+              int64_t s_head, int64_t s_batch, int box_rows, int box_heads = 1) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows > 0 ? rows : 1),
                         static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row) * 2, static_cast<cuuint64_t>(s_head) * 2,
                            static_cast<cuuint64_t>(s_batch) * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_heads), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -53,25 +53,37 @@ int num_sms() {
   return n > 0 ? n : 148;
 }
 
+enum Path { kPathSingle = 0, kPathPair = 1, kPathDecode = 2 };
+
 struct Geometry {
-  int G, R, nq, splits;
+  int G, R, nq, splits, path, ctas;
 };
 
-// Split-KV policy.  The host cannot see per-sequence lengths without a sync,
-// so the split count depends only on the shapes: grow splits while the grid is
-// under two waves, and for decode-like steps (one query tile per kv head) cap
-// a CTA at about 16 key tiles of the longest possible past.  Each split owns a
-// fixed range of the key-tile index space (see tiles.cuh).
+// Kernel path and work split for these sizes.  The host cannot see per-sequence
+// lengths without a sync, so every choice depends only on the shapes.
+//   pair   (D = 64/128, at least two query tiles): persistent CTAs, one per SM
+//          at most, balanced on the device by stream-K (no split-KV).
+//   decode (C = 1) and single-tile chunks: split-KV, each split owning a fixed
+//          range of the key-tile index space (see tiles.cuh); splits grow while
+//          the grid is under two waves, and decode caps a CTA at about 16 key
+//          tiles of the longest possible past.
 Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   Geometry g;
   g.G = Hq / Hkv;
   g.R = 128 / g.G;
   g.nq = (C + g.R - 1) / g.R;
+  g.ctas = 0;
+  const int sms = num_sms();
+  if (attn_uses_pair(D, g.nq) && !attn_uses_decode(D, C, g.G)) {
+    g.path = kPathPair;
+    g.splits = 1;
+    g.ctas = pair_ctas(B, Hkv, g.nq, P, C, sms);
+    return g;
+  }
+  g.path = attn_uses_decode(D, C, g.G) ? kPathDecode : kPathSingle;
   const int bn = attn_block_n(D);
   const int max_tiles = (P + bn - 1) / bn + (C + bn - 1) / bn;
-  const int per_kv = attn_uses_pair(D, g.nq) ? (g.nq + 1) / 2 : g.nq;
-  const long long ctas = static_cast<long long>(B) * Hkv * per_kv;
-  const int sms = num_sms();
+  const long long ctas = static_cast<long long>(B) * Hkv * g.nq;
   int s = 1;
   while (ctas * s < 2LL * sms && s * 2 <= max_tiles) s *= 2;
   if (g.nq == 1 && max_tiles > 32) s = max(s, (max_tiles + 15) / 16);
@@ -79,7 +91,8 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   return g;
 }
 
-size_t workspace_bytes(const Geometry& g, int B, int Hq, int D, int C) {
+size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
+  if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, g.nq, D, C, g.ctas).total;
   if (g.splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * C;
   const size_t o = static_cast<size_t>(g.splits) * rows * D * sizeof(float);
@@ -138,12 +151,12 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   if (static_cast<long long>(a->B) * a->Hq * a->C * a->D > (1LL << 40)) return CPA_ERR_SHAPE;
 
   const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
-  const size_t need = workspace_bytes(g, a->B, a->Hq, a->D, a->C);
+  const size_t need = workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C);
   if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)))
     return CPA_ERR_WORKSPACE;
 
   const int bn = attn_uses_decode(a->D, a->C, g.G) ? 64 : attn_block_n(a->D);
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   const cpa_cache* c = a->cache;
   const int64_t cs_ = static_cast<int64_t>(a->C) * a->D;
   if (!make_map(&maps[0], c->k, a->D, a->P, a->Hkv, a->B, c->stride_s, c->stride_h, c->stride_b, bn) ||
@@ -177,7 +190,26 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   p.out = static_cast<uint16_t*>(a->out);
   p.out_sel = a->out_sel;
   p.err = a->err;
-  if (g.splits > 1) {
+  p.k_new = static_cast<const uint16_t*>(a->k_new);
+  if (g.path == kPathPair) {
+    p.pairs = (g.nq + 1) / 2;
+    p.units = a->B * a->Hkv * p.pairs;
+    p.ctas = g.ctas;
+    uint8_t* w = static_cast<uint8_t*>(a->workspace);
+    const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, g.nq, a->D, a->C, g.ctas);
+    p.ustart = reinterpret_cast<int32_t*>(w + L.ustart);
+    p.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+    p.ptag = reinterpret_cast<int32_t*>(w + L.ptag);
+    p.q_rot = reinterpret_cast<uint16_t*>(w + L.q_rot);
+    p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
+    // chunk keys and queries come from the rotated copies the pre-pass writes
+    CUtensorMap pm[5] = {maps[0], maps[1], maps[2], maps[3], maps[4]};
+    if (!make_map(&pm[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn) ||
+        !make_map(&pm[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G))
+      return CPA_ERR_CUDA;
+    return launch_attn_pair5(pm, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+  } else if (g.splits > 1) {
     const size_t rows = static_cast<size_t>(a->B) * a->Hq * a->C;
     const size_t o = static_cast<size_t>(g.splits) * rows * a->D * sizeof(float);
     p.part_o = static_cast<float*>(a->workspace);
@@ -210,7 +242,7 @@ cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream) {
 
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P) {
   if (B < 1 || Hq < 1 || Hkv < 1 || C < 1 || P < 0 || Hq % Hkv || Hq / Hkv > 128 || !valid_d(D)) return 0;
-  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, D, C);
+  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, Hkv, D, C);
 }
 
 size_t cpa_cache_scratch_size(const cpa_cache* cache, int B, int Hkv, int D, int C) {

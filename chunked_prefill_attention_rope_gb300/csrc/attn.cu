@@ -490,8 +490,6 @@ cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream
   cudaError_t e;
   if (attn_uses_decode(p.D, p.C, p.G)) {
     e = launch_attn_decode(maps, p, stream);
-  } else if (attn_uses_pair(p.D, p.nq)) {
-    e = launch_attn_pair(maps, p, stream);
   } else {
     switch (p.D) {
       case 64: e = launch_attn_t<64, 128>(maps, p, stream); break;

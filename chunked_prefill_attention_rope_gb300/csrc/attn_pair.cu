@@ -1,11 +1,23 @@
-// Chunk-prefill attention for head dims 64 and 128 with two query tiles per CTA.
+// Chunk-prefill attention for head dims 64 and 128: two query tiles per work
+// unit, persistent CTAs with stream-K balancing.
 //
 // Same computation as attn_kernel ("functiongemma: chunk prefill-with-past
 // graph", Change: RoPE'd queries attend over past + chunk keys under an
-// additive mask), organised so the tensor core never waits for softmax:
+// additive mask), organised for the tensor core:
 //
-//   * A CTA owns 256 packed query rows of one (sequence, kv head), split into
-//     query tiles Q0 and Q1 of 128 rows; both use every K/V tile the CTA loads.
+//   * Work unit = 256 packed query rows of one (sequence, kv head): query tiles
+//     Q0 and Q1 of 128 rows that share every K/V tile.
+//   * plan_units_kernel counts the live key tiles of every unit (lengths live
+//     on the device) and prefix-sums them.  The persistent CTAs then split the
+//     concatenated tile sequence into equal contiguous ranges (stream-K): a CTA
+//     finishes whole units directly and writes partial results only for the at
+//     most two units cut at its range ends; merge_units_kernel combines those
+//     in fixed order and zero-fills units without live keys.
+//   * RoPE: rope_prep_kernel rotates the chunk's queries and keys once per call
+//     (coalesced, the same fp32 rounding as the cache append) into the
+//     workspace; the attention kernel TMA-loads rotated Q tiles and chunk-K
+//     tiles from there, so no tile is rotated twice and no load waits on a
+//     table lookup inside the pipeline.
 //   * TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them.  P
 //     (bf16) is written back over the first 64 columns of its S buffer and fed
 //     to the P V product straight from tensor memory.
@@ -16,8 +28,9 @@
 //     multiply-add per two scores (masked scores are -inf and give exactly 0).
 //
 // Warps: 0-3 softmax for Q0, 4-7 softmax for Q1 (warp w owns TMEM lanes
-// 32*(w%4)..+31), 8 TMA producer, 9 MMA issuer, 10-11 rotate raw chunk-K tiles
-// in shared memory.
+// 32*(w%4)..+31), 8 K/V TMA producer, 9 MMA issuer, 10 Q TMA loader.  Every
+// role walks the same segment sequence and counts tiles globally, so barrier
+// phases carry across unit boundaries.
 #include "tiles.cuh"
 
 namespace cpa {
@@ -25,7 +38,11 @@ namespace cpa {
 namespace {
 
 constexpr int kBN = 128;
-constexpr int kThreadsPair = 384;
+constexpr int kThreadsPair = 352;
+constexpr int kUnitRows = 256;
+// A unit switch (Q reload, epilogue, pipeline refill) costs about this many key
+// tiles; the stream-K split charges it to every non-empty unit.
+constexpr int kSwitchCost = 2;
 
 template <int D>
 struct PairCfg {
@@ -42,8 +59,8 @@ struct PairCfg {
 };
 
 struct __align__(8) PairBars {
-  uint64_t k_full[4], v_full[4], kv_empty[4], k_rot[4];
-  uint64_t s_full[2], p_full[2], o_done[2], q_ready[2];
+  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2], q_full[2], q_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -54,13 +71,149 @@ constexpr int pair_smem_bytes() {
   return PairCfg<D>::kBars + static_cast<int>(sizeof(PairBars)) + 1024;
 }
 
+struct Unit {
+  int b, kvh, pair;
+};
+
+__device__ __forceinline__ Unit unit_of(const AttnParams& p, int u) {
+  Unit x;
+  x.pair = u % p.pairs;
+  x.kvh = (u / p.pairs) % p.Hkv;
+  x.b = u / (p.pairs * p.Hkv);
+  return x;
+}
+
+__device__ __forceinline__ TilePlan unit_plan(const AttnParams& p, const Unit& x) {
+  const int i_min = x.pair * 2 * p.R;
+  const int i_max = min(i_min + 2 * p.R, p.C) - 1;
+  return plan_whole<kBN>(p, x.b, i_min, i_max);
+}
+
+// First tile of CTA c's range in the concatenated tile sequence of T tiles.
+__device__ __forceinline__ long long cta_lo(long long T, int c, int ctas) { return T * c / ctas; }
+
+// Largest u in [0, U) with start[u] <= x (the unit holding tile x when x < T).
+__device__ __forceinline__ int unit_at(const int32_t* start, int U, long long x) {
+  int lo = 0, hi = U - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (start[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Walks the (unit, first tile, end tile) segments of CTA c's range of cost
+// positions.
+struct SegWalk {
+  const int32_t* start;
+  int U, u;
+  long long lo, hi;
+  __device__ __forceinline__ void init(const AttnParams& p, int c) {
+    start = p.ustart;
+    U = p.units;
+    const long long T = start[U];
+    lo = cta_lo(T, c, p.ctas);
+    hi = cta_lo(T, c + 1, p.ctas);
+    u = lo < hi ? unit_at(start, U, lo) : U;
+  }
+  // Next segment holding at least one key tile; false when the range is
+  // exhausted.  Unit u spans cost positions [start[u], start[u+1]): first the
+  // switch cost, then one position per key tile.
+  __device__ __forceinline__ bool next(int& unit, int& a, int& e) {
+    while (u < U && start[u] < hi) {
+      const long long t0 = start[u] + kSwitchCost, s1 = start[u + 1];
+      const int cur = u++;
+      const long long aa = lo > t0 ? lo : t0;
+      const long long ee = hi < s1 ? hi : s1;
+      if (ee > aa) {
+        unit = cur;
+        a = static_cast<int>(aa - t0);
+        e = static_cast<int>(ee - t0);
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
 }  // namespace
+
+// Rotated copies of the chunk's queries and keys (RoPE from the per-row
+// cos/sin tables, fp32 products and sums without fused multiply-add, bf16
+// round-to-nearest-even: the bytes the cache append writes for K).
+__global__ void __launch_bounds__(256) rope_prep_kernel(const AttnParams p) {
+  const int D = p.D;
+  const int HP = D / 16;  // 8-element chunk pairs (d, d + D/2) per row
+  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.C;
+  const long long total = (rows_q + static_cast<long long>(p.B) * p.Hkv * p.C) * HP;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int kc = static_cast<int>(it % HP);
+    const long long row = it / HP;  // q rows first, then chunk-key rows
+    const bool is_q = row < rows_q;
+    const long long r = is_q ? row : row - rows_q;
+    const int i = static_cast<int>(r % p.C);
+    const int b = static_cast<int>(r / p.C / (is_q ? p.Hq : p.Hkv));
+    const uint16_t* src = (is_q ? p.q : p.k_new) + r * D;
+    uint16_t* dst = (is_q ? p.q_rot : p.k_rot) + r * D;
+    uint4 lo = *reinterpret_cast<const uint4*>(src + kc * 8);
+    uint4 hi = *reinterpret_cast<const uint4*>(src + D / 2 + kc * 8);
+    const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
+    const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
+    rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
+    *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
+  }
+}
+
+// Cost of every unit (its live key tiles plus the switch cost) and the
+// exclusive prefix sum of the costs (one CTA).
+__global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  for (int base = 0; base < p.units; base += 1024) {
+    const int u = base + threadIdx.x;
+    int n = 0;
+    if (u < p.units) {
+      n = unit_plan(p, unit_of(p, u)).count();
+      if (n > 0) n += kSwitchCost;
+    }
+    int incl = n;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (u < p.units) p.ustart[u] = before + incl - n;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = before + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.ustart[p.units] = carry;
+}
 
 template <int D, bool EXPLICIT>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                      const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
-                     const AttnParams p) {
+                     const __grid_constant__ CUtensorMap map_q, const AttnParams p) {
   using CF = PairCfg<D>;
   constexpr int NS = CF::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -70,34 +223,31 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int pair = blockIdx.x / p.splits;
-  const int split = blockIdx.x % p.splits;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
-  const int i_min = pair * 2 * p.R;
-  const int i_max = min(i_min + 2 * p.R, p.C) - 1;
-  const TilePlan tp = plan_tiles<kBN>(p, b, i_min, i_max, split);
-  const int nt = tp.count();
+  const int cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->k_rot[s], 64);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->o_done[s], 1);
-      mbar_init(&bars->q_ready[s], 128);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_free[s], 128);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
-    if (kvh == 0 && blockIdx.x == 0) {
-      if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
-      if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+    p.ptag[2 * cta] = -1;  // no partial result of this call yet
+    p.ptag[2 * cta + 1] = -1;
+    if (cta == 0) {
+      for (int b = 0; b < p.B; ++b) {
+        if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
+        if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+      }
     }
   }
   if (warp == 9) {
@@ -109,34 +259,41 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t tmem = bars->tmem_base;
   uint8_t* sK = smem + CF::kK;
   uint8_t* sV = smem + CF::kV;
+  SegWalk walk;
+  walk.init(p, cta);
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nt > 0) {
+    if (lane == 0) {
       prefetch_tensormap(&map_kc);
       prefetch_tensormap(&map_vc);
       prefetch_tensormap(&map_kn);
       prefetch_tensormap(&map_vn);
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int st = j % NS;
-        if (!mbar_wait(&bars->kv_empty[st], ((j / NS) + 1) & 1, abort)) break;
-        const int t = tp.index(j);
-        const bool chunk = t < tp.Tc;
-        const int base = (chunk ? t : t - tp.Tc) * kBN;
-        const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
-        const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
-        mbar_arrive_expect_tx(&bars->k_full[st], CF::kKBytes);
+      int g = 0;  // tiles issued (chunk keys come from the rotated copy behind map_kn)
+      bool ok = true;
+      int unit, a, e;
+      while (ok && walk.next(unit, a, e)) {
+        const Unit x = unit_of(p, unit);
+        const TilePlan tp = unit_plan(p, x);
+        for (int j = a; j < e; ++j, ++g) {
+          const int st = g % NS;
+          if (!(ok = mbar_wait(&bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
+          const int t = tp.index(j);
+          const bool chunk = t < tp.Tc;
+          const int base = (chunk ? t : t - tp.Tc) * kBN;
+          const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
+          const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
+          mbar_arrive_expect_tx(&bars->k_full[st], CF::kKBytes);
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(sK + st * CF::kKBytes + blk * kBN * 128, mk, &bars->k_full[st], blk * 64, base, kvh, b);
-        mbar_arrive_expect_tx(&bars->v_full[st], CF::kVBytes);
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_4d(sK + st * CF::kKBytes + blk * kBN * 128, mk, &bars->k_full[st], blk * 64, base, x.kvh, x.b);
+          mbar_arrive_expect_tx(&bars->v_full[st], CF::kVBytes);
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(sV + st * CF::kVBytes + blk * kBN * 128, mv, &bars->v_full[st], blk * 64, base, kvh, b);
-        issued = j + 1;
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_4d(sV + st * CF::kVBytes + blk * kBN * 128, mv, &bars->v_full[st], blk * 64, base, x.kvh, x.b);
+        }
       }
-      for (int j = max(0, issued - NS); j < issued; ++j) {  // let copies in flight land
+      for (int j = max(0, g - NS); j < g; ++j) {  // let copies in flight land
         const int st = j % NS;
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(&bars->v_full[st], (j / NS) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
@@ -149,14 +306,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(128, kBN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
       const uint32_t q_addr = smem_u32(smem + CF::kQ);
-      bool ok = nt > 0 && mbar_wait(&bars->q_ready[0], 0, abort) && mbar_wait(&bars->q_ready[1], 0, abort);
-      auto k_ready = [&](int j) -> bool {
-        const int st = j % NS;
-        const bool chunk = tp.index(j) < tp.Tc;
-        return mbar_wait(chunk ? &bars->k_rot[st] : &bars->k_full[st], (j / NS) & 1, abort);
+      int g = 0, seg = 0;
+      bool ok = true;
+      auto k_ready = [&](const TilePlan&, int, int gg) -> bool {
+        return mbar_wait(&bars->k_full[gg % NS], (gg / NS) & 1, abort);
       };
-      auto issue_qk = [&](int i, int j) {
-        const uint32_t k_addr = smem_u32(sK + (j % NS) * CF::kKBytes);
+      auto issue_qk = [&](int i, int gg) {
+        const uint32_t k_addr = smem_u32(sK + (gg % NS) * CF::kKBytes);
         const uint32_t qa = q_addr + i * CF::kQBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -166,277 +322,276 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
         mma_commit(&bars->s_full[i]);
       };
-      auto issue_pv = [&](int i, int j) {
-        const uint32_t v_addr = smem_u32(sV + (j % NS) * CF::kVBytes);
+      auto issue_pv = [&](int i, int gg, bool first) {
+        const uint32_t v_addr = smem_u32(sV + (gg % NS) * CF::kVBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kBN * 128, 1024);
-          mma_bf16_ts(tmem + CF::kOCol + i * D, tmem + i * kBN + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + CF::kOCol + i * D, tmem + i * kBN + kk * 8, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
       };
-      if (ok && (ok = k_ready(0))) {
+      int unit, a, e;
+      while (ok && walk.next(unit, a, e)) {
+        const TilePlan tp = unit_plan(p, unit_of(p, unit));
+        const int n = e - a;
+        if (!(ok = k_ready(tp, a, g) && mbar_wait(&bars->q_full[0], seg & 1, abort))) break;
         tc_fence_after();
-        issue_qk(0, 0);
-        issue_qk(1, 0);
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        const int st = j % NS;
-        if (!(ok = mbar_wait(&bars->p_full[0], j & 1, abort) && mbar_wait(&bars->v_full[st], (j / NS) & 1, abort)))
-          break;
+        issue_qk(0, g);
+        if (!(ok = mbar_wait(&bars->q_full[1], seg & 1, abort))) break;
         tc_fence_after();
-        issue_pv(0, j);
-        if (j + 1 == nt) mma_commit(&bars->o_done[0]);
-        if (j + 1 < nt) {
-          if (!(ok = k_ready(j + 1))) break;
+        issue_qk(1, g);
+        for (int jj = 0; jj < n; ++jj) {
+          const int gt = g + jj;
+          const int st = gt % NS;
+          if (!(ok = mbar_wait(&bars->p_full[0], gt & 1, abort) && mbar_wait(&bars->v_full[st], (gt / NS) & 1, abort)))
+            break;
           tc_fence_after();
-          issue_qk(0, j + 1);
+          issue_pv(0, gt, jj == 0);
+          if (jj + 1 == n) {
+            mma_commit(&bars->o_done[0]);
+          } else {
+            if (!(ok = k_ready(tp, a + jj + 1, gt + 1))) break;
+            tc_fence_after();
+            issue_qk(0, gt + 1);
+          }
+          if (!(ok = mbar_wait(&bars->p_full[1], gt & 1, abort))) break;
+          tc_fence_after();
+          issue_pv(1, gt, jj == 0);
+          mma_commit(&bars->kv_empty[st]);
+          if (jj + 1 == n) mma_commit(&bars->o_done[1]);
+          else issue_qk(1, gt + 1);
         }
-        if (!(ok = mbar_wait(&bars->p_full[1], j & 1, abort))) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        mma_commit(&bars->kv_empty[st]);
-        if (j + 1 == nt) mma_commit(&bars->o_done[1]);
-        if (j + 1 < nt) issue_qk(1, j + 1);
+        g += n;
+        ++seg;
       }
       mma_commit(&bars->mma_done);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(&bars->mma_done, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
     __syncwarp();
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ chunk-K rotation
-    const int tid = threadIdx.x - 320;  // 0..63
-    for (int j = 0; j < nt; ++j) {
-      const int t = tp.index(j);
-      if (t >= tp.Tc) break;  // chunk tiles come first
-      const int st = j % NS;
-      if (!warp_all(mbar_wait(&bars->k_full[st], (j / NS) & 1, abort))) break;
-      uint8_t* kt = sK + st * CF::kKBytes;
-      const int base = t * kBN;
-      for (int item = tid; item < kBN * (D / 16); item += 64) {
-        const int r = item / (D / 16);
-        const int kc = item % (D / 16);
-        const int row = base + r;
-        if (row >= p.C) continue;
-        const int kh = kc + D / 16;
-        uint4* plo = reinterpret_cast<uint4*>(kt + (kc / 8) * (kBN * 128) + sw128(r, kc % 8));
-        uint4* phi = reinterpret_cast<uint4*>(kt + (kh / 8) * (kBN * 128) + sw128(r, kh % 8));
-        uint4 lo = *plo, hi = *phi;
-        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + row) * D;
-        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + row) * D;
-        rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-        *plo = lo;
-        *phi = hi;
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ Q TMA loader
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      const uint32_t q_bytes = (D / 64) * 128 * p.R * p.G;
+      int seg = 0;
+      bool ok = true;
+      int unit, a, e;
+      while (ok && walk.next(unit, a, e)) {
+        const Unit x = unit_of(p, unit);
+        for (int qi = 0; qi < 2 && ok; ++qi) {
+          // the previous segment's S = Q K products of this tile have completed
+          if (!(ok = mbar_wait(&bars->q_free[qi], (seg + 1) & 1, abort))) break;
+          mbar_arrive_expect_tx(&bars->q_full[qi], q_bytes);
+          uint8_t* sQ = smem + CF::kQ + qi * CF::kQBytes;
+#pragma unroll
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_4d(sQ + blk * (128 * 128), &map_q, &bars->q_full[qi], blk * 64, (x.pair * 2 + qi) * p.R,
+                        x.kvh * p.G, x.b);
+        }
+        ++seg;
       }
-      fence_async_smem();
-      mbar_arrive(&bars->k_rot[st]);
+      for (int qi = 0; qi < 2 && seg > 0; ++qi) {  // let copies in flight land
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars->q_full[qi], (seg - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax (query tile qi)
     const int qi = warp / 4;
-    const int tid = threadIdx.x - qi * 128;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lanes = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t s_col = tmem + lanes + qi * kBN;
     const uint32_t o_col = tmem + lanes + CF::kOCol + qi * D;
-    const int qt = pair * 2 + qi;
-    const int g = row / p.R;
-    const int i = qt * p.R + row % p.R;
-    const bool valid = g < p.G && i < p.C;
-    const int h = kvh * p.G + (valid ? g : 0);
-
-    // rotated Q rows into the swizzled K-major operand tile
-    uint8_t* sQ = smem + CF::kQ + qi * CF::kQBytes;
-    for (int item = tid; item < 128 * (D / 16); item += 128) {
-      const int r = item / (D / 16);
-      const int kc = item % (D / 16);
-      const int rg = r / p.R;
-      const int ri = qt * p.R + r % p.R;
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (rg < p.G && ri < p.C) {
-        const size_t off = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + rg) * p.C + ri) * D;
-        lo = *reinterpret_cast<const uint4*>(p.q + off + kc * 8);
-        hi = *reinterpret_cast<const uint4*>(p.q + off + D / 2 + kc * 8);
-        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-        rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-      }
-      const int kh = kc + D / 16;
-      *reinterpret_cast<uint4*>(sQ + (kc / 8) * (128 * 128) + sw128(r, kc % 8)) = lo;
-      *reinterpret_cast<uint4*>(sQ + (kh / 8) * (128 * 128) + sw128(r, kh % 8)) = hi;
-    }
-    fence_async_smem();
-    mbar_arrive(&bars->q_ready[qi]);
-
-    RowSpan span;
-    span.init(p, tp, i, valid);
-    const float* mrow = nullptr;
-    if (EXPLICIT && valid)
-      mrow = p.mask + ((static_cast<size_t>(b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C);
     const float sl2 = p.sl2;
-    float m_run = kMaskedLog2, l_run = 0.f;
+    int g = 0, seg = 0;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int t = tp.index(j);
-      const bool chunk = t < tp.Tc;
-      const int base = (chunk ? t : t - tp.Tc) * kBN;
-      int lo, hi;
-      span.tile(chunk, base, lo, hi);
-      const float* mp = nullptr;
-      int lim = 0;
-      if (EXPLICIT) {
-        lim = chunk ? p.C - base : p.P - base;
-        if (mrow) mp = mrow + (chunk ? p.P + base : base);
-      }
-      if (!(ok = warp_all(mbar_wait(&bars->s_full[qi], j & 1, abort)))) break;
-      tc_fence_after();
+    int unit, a, e;
+    while (ok && walk.next(unit, a, e)) {
+      const Unit x = unit_of(p, unit);
+      const TilePlan tp = unit_plan(p, x);
+      const int qt = x.pair * 2 + qi;
+      const int gr = row / p.R;
+      const int i = qt * p.R + row % p.R;
+      const bool valid = gr < p.G && i < p.C;
+      const int h = x.kvh * p.G + (valid ? gr : 0);
 
-      // Scores of this row.  Implicit mask: one batch of TMEM loads, masked keys
-      // set to -inf (they give exactly 0 below).  Explicit mask: the row max of
-      // scale*s + mask (in log2 units), chunk by chunk.
-      float sc[kBN];
-      float m_tile;
-      if (!EXPLICIT) {
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(s_col + 32 * c, sc + 32 * c);
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
-        if (__any_sync(0xffffffffu, lo > 0 || hi < kBN)) {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) sc[e] = (e >= lo && e < hi) ? sc[e] : -INFINITY;
+      RowSpan span;
+      span.init(p, tp, i, valid);
+      const float* mrow = nullptr;
+      if (EXPLICIT && valid)
+        mrow = p.mask + ((static_cast<size_t>(x.b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C);
+      float m_run = kMaskedLog2, l_run = 0.f;
+      const int n = e - a;
+      for (int jj = 0; jj < n; ++jj) {
+        const int gt = g + jj;
+        const int t = tp.index(a + jj);
+        const bool chunk = t < tp.Tc;
+        const int base = (chunk ? t : t - tp.Tc) * kBN;
+        int lo, hi;
+        span.tile(chunk, base, lo, hi);
+        const float* mp = nullptr;
+        int lim = 0;
+        if (EXPLICIT) {
+          lim = chunk ? p.C - base : p.P - base;
+          if (mrow) mp = mrow + (chunk ? p.P + base : base);
         }
-        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+        if (!(ok = warp_all(mbar_wait(&bars->s_full[qi], gt & 1, abort)))) break;
+        tc_fence_after();
+        if (jj + 1 == n) mbar_arrive(&bars->q_free[qi]);  // last S = Q K of the segment is done
+
+        // Scores of this row.  Implicit mask: one batch of TMEM loads, masked
+        // keys set to -inf (they give exactly 0 below).  Explicit mask: the row
+        // max of scale*s + mask (in log2 units), chunk by chunk.
+        float sc[kBN];
+        float m_tile;
+        if (!EXPLICIT) {
 #pragma unroll
-        for (int e = 0; e < kBN; e += 8) {
-          m0 = fmax3(m0, sc[e], sc[e + 1]);
-          m1 = fmax3(m1, sc[e + 2], sc[e + 3]);
-          m2 = fmax3(m2, sc[e + 4], sc[e + 5]);
-          m3 = fmax3(m3, sc[e + 6], sc[e + 7]);
+          for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(s_col + 32 * c, sc + 32 * c);
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
+          if (__any_sync(0xffffffffu, lo > 0 || hi < kBN)) {
+#pragma unroll
+            for (int q = 0; q < kBN; ++q) sc[q] = (q >= lo && q < hi) ? sc[q] : -INFINITY;
+          }
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kBN; q += 8) {
+            m0 = fmax3(m0, sc[q], sc[q + 1]);
+            m1 = fmax3(m1, sc[q + 2], sc[q + 3]);
+            m2 = fmax3(m2, sc[q + 4], sc[q + 5]);
+            m3 = fmax3(m3, sc[q + 6], sc[q + 7]);
+          }
+          const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+          m_tile = (mt == -INFINITY) ? kMaskedLog2 : __fmul_rn(mt, sl2);
+        } else {
+          float mt = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(s_col + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int k = 32 * c + q;
+              const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
+              mt = fmaxf(mt, __fmaf_rn(__uint_as_float(r[q]), sl2, __fmul_rn(mv, kLog2e)));
+            }
+          }
+          m_tile = mt;
         }
-        const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-        m_tile = (mt == -INFINITY) ? kMaskedLog2 : __fmul_rn(mt, sl2);
-      } else {
-        float mt = -INFINITY;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool rescale = m_new > m_run + 8.f;
+        float factor = 1.f;
+        if (rescale) {
+          factor = fast_exp2(m_run - m_new);
+          m_run = m_new;
+        }
+        const bool live = m_run > kEmptyRow;
+        if (jj > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O holds every earlier P V (the S = Q K that signalled s_full was issued after them)
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_col + 32 * c, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
+            tmem_st32(o_col + 32 * c, o);
+          }
+        }
+        // P = 2^(scale*log2e*s - m), summed in one fixed order, written over S as bf16
+        float2 accA = make_float2(0.f, 0.f), accB = accA;
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(s_col + 32 * c, r);
-          tmem_ld_wait(r);
+          float* pv = sc + 32 * c;
+          if (!EXPLICIT) {
+            const float nm = live ? -m_run : -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int k = 32 * c + e;
-            const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
-            mt = fmaxf(mt, __fmaf_rn(__uint_as_float(r[e]), sl2, __fmul_rn(mv, kLog2e)));
+            for (int q = 0; q < 32; q += 2) {
+              const float2 y = ffma2(make_float2(pv[q], pv[q + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+              pv[q] = fast_exp2(y.x);
+              pv[q + 1] = fast_exp2(y.y);
+            }
+          } else {
+            uint32_t r[32];
+            tmem_ld32(s_col + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int k = 32 * c + q;
+              const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
+              pv[q] = live ? fast_exp2(__fmaf_rn(__uint_as_float(r[q]), sl2, __fadd_rn(__fmul_rn(mv, kLog2e), -m_run)))
+                           : 0.f;
+            }
           }
-        }
-        m_tile = mt;
-      }
-      const float m_new = fmaxf(m_run, m_tile);
-      const bool rescale = m_new > m_run + 8.f;
-      float factor = 1.f;
-      if (rescale) {
-        factor = fast_exp2(m_run - m_new);
-        m_run = m_new;
-      }
-      const bool live = m_run > kEmptyRow;
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds every earlier P V (the S = Q K that signalled s_full was issued after them)
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_col + 32 * c, o);
-          tmem_ld_wait(o);
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st32(o_col + 32 * c, o);
-        }
-      }
-      // P = 2^(scale*log2e*s - m), summed in one fixed order, written over S as bf16
-      float2 accA = make_float2(0.f, 0.f), accB = accA;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        float* pv = sc + 32 * c;
-        if (!EXPLICIT) {
-          const float nm = live ? -m_run : -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 x = ffma2(make_float2(pv[e], pv[e + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-            pv[e] = fast_exp2(x.x);
-            pv[e + 1] = fast_exp2(x.y);
+          for (int q = 0; q < 32; q += 4) {
+            accA = fadd2(accA, make_float2(pv[q], pv[q + 1]));
+            accB = fadd2(accB, make_float2(pv[q + 2], pv[q + 3]));
+            w[q / 2] = pack_bf16x2(pv[q], pv[q + 1]);
+            w[q / 2 + 1] = pack_bf16x2(pv[q + 2], pv[q + 3]);
           }
-        } else {
-          uint32_t r[32];
-          tmem_ld32(s_col + 32 * c, r);
-          tmem_ld_wait(r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int k = 32 * c + e;
-            const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
-            pv[e] = live ? fast_exp2(__fmaf_rn(__uint_as_float(r[e]), sl2, __fadd_rn(__fmul_rn(mv, kLog2e), -m_run)))
-                         : 0.f;
-          }
+          tmem_st16(s_col + 16 * c, w);
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          accA = fadd2(accA, make_float2(pv[e], pv[e + 1]));
-          accB = fadd2(accB, make_float2(pv[e + 2], pv[e + 3]));
-          w[e / 2] = pack_bf16x2(pv[e], pv[e + 1]);
-          w[e / 2 + 1] = pack_bf16x2(pv[e + 2], pv[e + 3]);
-        }
-        tmem_st16(s_col + 16 * c, w);
+        const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
+        tmem_st_wait();
+        l_run = __fmaf_rn(l_run, factor, sum);
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[qi]);
       }
-      const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
-      tmem_st_wait();
-      l_run = __fmaf_rn(l_run, factor, sum);
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[qi]);
-    }
+      if (!ok) break;
 
-    // ---------------------------------------------------------- epilogue
-    if (ok && nt > 0) ok = warp_all(mbar_wait(&bars->o_done[qi], 0, abort));
-    tc_fence_after();
-    const bool empty = !(nt > 0 && ok && m_run > kEmptyRow);
-    const float inv_l = empty ? 0.f : 1.f / l_run;
-    const int sel = valid ? (p.sel_row ? p.sel_row[b] : tp.n - 1) : -1;
-    const size_t orow = (static_cast<size_t>(b) * p.Hq + h) * p.C + i;
+      // -------------------------------------------------------- segment epilogue
+      if (!(ok = warp_all(mbar_wait(&bars->o_done[qi], seg & 1, abort)))) break;
+      tc_fence_after();
+      const bool whole = a == 0 && e == tp.count();
+      const bool empty = !(m_run > kEmptyRow);
+      const float inv_l = empty ? 0.f : 1.f / l_run;
+      const int sel = valid ? (p.sel_row ? p.sel_row[x.b] : tp.n - 1) : -1;
+      const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h) * p.C + i;
+      // only a CTA's first and last segments can be partial: slots 0 and 1
+      const int which = seg == 0 ? 0 : 1;
+      const size_t slot = (static_cast<size_t>(cta) * 2 + which) * kUnitRows + qi * 128 + row;
+      if (!whole && qi == 0 && row == 0) p.ptag[2 * cta + which] = unit;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o32[32];
-      if (nt > 0) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o32[32];
         tmem_ld32(o_col + 32 * c, o32);
         tmem_ld_wait(o32);
-      }
-      float o[32];
+        float o[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : __uint_as_float(o32[e]) * inv_l;
-      if (!valid) continue;
-      if (p.part_o) {
-        float* dst = p.part_o + (static_cast<size_t>(split) * p.B * p.Hq * p.C + orow) * D + 32 * c;
+        for (int q = 0; q < 32; ++q) o[q] = empty ? 0.f : __uint_as_float(o32[q]) * inv_l;
+        if (!valid) continue;
+        if (!whole) {
+          float* dst = p.part_o + slot * D + 32 * c;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-      } else {
-        uint16_t* dst = p.out + orow * D + 32 * c;
+          for (int q = 0; q < 32; q += 4)
+            *reinterpret_cast<float4*>(dst + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+        } else {
+          uint16_t* dst = p.out + orow * D + 32 * c;
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 wv;
-          wv.x = pack_bf16x2(o[e + 0], o[e + 1]);
-          wv.y = pack_bf16x2(o[e + 2], o[e + 3]);
-          wv.z = pack_bf16x2(o[e + 4], o[e + 5]);
-          wv.w = pack_bf16x2(o[e + 6], o[e + 7]);
-          *reinterpret_cast<uint4*>(dst + e) = wv;
+          for (int q = 0; q < 32; q += 8) {
+            uint4 wv;
+            wv.x = pack_bf16x2(o[q + 0], o[q + 1]);
+            wv.y = pack_bf16x2(o[q + 2], o[q + 3]);
+            wv.z = pack_bf16x2(o[q + 4], o[q + 5]);
+            wv.w = pack_bf16x2(o[q + 6], o[q + 7]);
+            *reinterpret_cast<uint4*>(dst + q) = wv;
+          }
+          if (p.out_sel && i == sel) {
+            float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h) * D + 32 * c;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<float4*>(sd + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+          }
         }
-        if (p.out_sel && i == sel) {
-          float* sd = p.out_sel + (static_cast<size_t>(b) * p.Hq + h) * D + 32 * c;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(sd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-        }
       }
+      if (valid && !whole) p.part_lse[slot] = empty ? -INFINITY : m_run + __log2f(l_run);
+      g += n;
+      ++seg;
     }
-    if (valid && p.part_lse)
-      p.part_lse[static_cast<size_t>(split) * p.B * p.Hq * p.C + orow] = empty ? -INFINITY : m_run + __log2f(l_run);
   }
 
   __syncthreads();
@@ -445,6 +600,103 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Final rows of units cut between CTAs (merged in CTA order) and of units with
+// no live key tile (zeros).  One CTA per unit; whole units exit at once.
+constexpr int kMaxCtas = 256;
+
+__global__ void __launch_bounds__(1024) merge_units_kernel(const AttnParams p) {
+  __shared__ int piece_slot[kMaxCtas];  // partial-result slot of each piece, in CTA order
+  __shared__ int n_pieces;
+  const int unit = blockIdx.x;
+  const long long s0 = p.ustart[unit], s1 = p.ustart[unit + 1];
+  const long long T = p.ustart[p.units];
+  if (threadIdx.x == 0) {
+    // CTA c covers cost positions [floor(c T / ctas), floor((c+1) T / ctas));
+    // the last CTA whose range starts at or before x is floor(((x + 1) ctas - 1) / T).
+    int np = 0;
+    if (s1 > s0) {
+      const int c_first = static_cast<int>(((s0 + 1) * p.ctas - 1) / T);
+      const int c_last = static_cast<int>((s1 * p.ctas - 1) / T);
+      for (int c = c_first; c <= c_last; ++c) {
+        if (p.ptag[2 * c] == unit) piece_slot[np++] = 2 * c;
+        else if (p.ptag[2 * c + 1] == unit) piece_slot[np++] = 2 * c + 1;
+      }
+      if (np == 0) np = -1;  // one CTA did the whole unit and wrote it already
+    }
+    n_pieces = np;
+  }
+  __syncthreads();
+  const int np = n_pieces;
+  if (np < 0) return;
+  const Unit x = unit_of(p, unit);
+  const int D = p.D;
+  const int n_real = p.n_real ? min(max(p.n_real[x.b], 0), p.C) : p.C;
+  const int sel = p.sel_row ? p.sel_row[x.b] : n_real - 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int per = D / 32;
+  for (int r = warp; r < kUnitRows; r += 32) {
+    const int qi = r / 128, rr = r % 128;
+    const int gr = rr / p.R;
+    const int i = (x.pair * 2 + qi) * p.R + rr % p.R;
+    if (gr >= p.G || i >= p.C) continue;
+    const int h = x.kvh * p.G + gr;
+    const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h) * p.C + i;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float lmax = -INFINITY;
+    for (int k = 0; k < np; ++k)
+      lmax = fmaxf(lmax, p.part_lse[static_cast<size_t>(piece_slot[k]) * kUnitRows + r]);
+    float wsum = 0.f;
+    if (lmax != -INFINITY) {
+      for (int k = 0; k < np; ++k) {
+        const size_t sidx = static_cast<size_t>(piece_slot[k]) * kUnitRows + r;
+        const float ls = p.part_lse[sidx];
+        if (ls == -INFINITY) continue;
+        const float w = fast_exp2(ls - lmax);
+        wsum += w;
+        const float* src = p.part_o + sidx * D + lane * per;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < per) acc[q] = __fmaf_rn(w, src[q], acc[q]);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; q += 2) {
+      if (q < per) {
+        const float o0 = acc[q] * inv, o1 = acc[q + 1] * inv;
+        *reinterpret_cast<uint32_t*>(p.out + orow * D + lane * per + q) = pack_bf16x2(o0, o1);
+        if (p.out_sel && i == sel) {
+          float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h) * D + lane * per + q;
+          sd[0] = o0;
+          sd[1] = o1;
+        }
+      }
+    }
+  }
+}
+
+int pair_ctas(int B, int Hkv, int nq, int P, int C, int num_sms) {
+  const long long units = static_cast<long long>(B) * Hkv * ((nq + 1) / 2);
+  const long long max_tiles = units * ((P + kBN - 1) / kBN + (C + kBN - 1) / kBN);
+  const long long cap = num_sms < kMaxCtas ? num_sms : kMaxCtas;
+  return static_cast<int>(max(1LL, min(cap, max_tiles)));
+}
+
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int nq, int D, int C, int ctas) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t units = static_cast<size_t>(B) * Hkv * ((nq + 1) / 2);
+  PairWorkspace w;
+  size_t off = 0;
+  w.ustart = off; off += al((units + 1) * sizeof(int32_t));
+  w.part_o = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * D * sizeof(float));
+  w.part_lse = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * sizeof(float));
+  w.ptag = off; off += al(static_cast<size_t>(ctas) * 2 * sizeof(int32_t));
+  w.q_rot = off; off += al(static_cast<size_t>(B) * Hq * C * D * 2);
+  w.k_rot = off; off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
+  w.total = off;
+  return w;
 }
 
 template <int D, bool EXPLICIT>
@@ -457,13 +709,16 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int pairs = (p.nq + 1) / 2;
-  dim3 grid(pairs * p.splits, p.Hkv, p.B);
-  kern<<<grid, kThreadsPair, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  const long long items = (static_cast<long long>(p.B) * (p.Hq + p.Hkv) * p.C) * (p.D / 16);
+  const int blocks = static_cast<int>(min(static_cast<long long>(65535) * 4, (items + 255) / 256));
+  rope_prep_kernel<<<blocks, 256, 0, stream>>>(p);
+  plan_units_kernel<<<1, 1024, 0, stream>>>(p);
+  kern<<<p.ctas, kThreadsPair, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  merge_units_kernel<<<p.units, 1024, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_pair(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   const bool ex = p.mask != nullptr;
   switch (p.D) {
     case 64: return ex ? launch_pair_t<64, true>(maps, p, stream) : launch_pair_t<64, false>(maps, p, stream);

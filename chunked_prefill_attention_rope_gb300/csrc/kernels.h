@@ -23,12 +23,30 @@ struct AttnParams {
   float* part_o;    // split-KV partials [splits][B][Hq][C][D] or null
   float* part_lse;  // [splits][B][Hq][C]
   int32_t* err;
+  // persistent stream-K path (two query tiles per work unit)
+  int32_t* ustart;  // [units + 1] exclusive prefix sum of live tiles per unit
+  int units;        // B * Hkv * pairs
+  int pairs;        // query-tile pairs per (sequence, kv head)
+  int ctas;         // persistent CTAs
+  const uint16_t* k_new;  // chunk keys before RoPE [B, Hkv, C, D]
+  uint16_t* q_rot;        // rotated queries [B, Hq, C, D] (workspace)
+  uint16_t* k_rot;        // rotated chunk keys [B, Hkv, C, D] (workspace)
+  int32_t* ptag;          // [2 * ctas] unit of each CTA's partial slots (-1: none)
 };
+
+// Persistent stream-K layout: number of CTAs and workspace bytes for these sizes.
+int pair_ctas(int B, int Hkv, int nq, int P, int C, int num_sms);
+struct PairWorkspace {
+  size_t ustart, part_o, part_lse, ptag, q_rot, k_rot, total;
+};
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int nq, int D, int C, int ctas);
+// maps for the pair path: cache K, cache V, rotated chunk K, chunk V, rotated Q
+// (dims {D, C, Hq, B}, box {64, R, G, 1}).
+cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 
 int attn_block_n(int D);
 // True when the two-query-tile kernel (256 packed rows per CTA) serves these sizes.
 inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >= 2; }
-cudaError_t launch_attn_pair(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 // True when the warp-MMA decode kernel (64-key tiles, G <= 16 rows) serves these sizes.
 inline bool attn_uses_decode(int D, int C, int G) { return C == 1 && (D == 64 || D == 128) && G <= 16; }
 cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);

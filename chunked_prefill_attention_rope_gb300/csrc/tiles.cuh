@@ -27,9 +27,11 @@ struct TilePlan {
   __device__ __forceinline__ int index(int q) const { return q < ce - cb ? cb + q : pb + (q - (ce - cb)); }
 };
 
-// Live key tiles for query rows [i_min, i_max] of sequence b, restricted to split `split`.
+// Live key tiles for query rows [i_min, i_max] of sequence b, restricted to the
+// tile index range [r0, r1).
 template <int BN>
-__device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int i_min, int i_max, int split) {
+__device__ __forceinline__ TilePlan plan_tiles_range(const AttnParams& p, int b, int i_min, int i_max, long long r0,
+                                                     long long r1) {
   TilePlan t;
   int L = p.past_len ? p.past_len[b] : p.P;
   int n = p.n_real ? p.n_real[b] : p.C;
@@ -49,14 +51,26 @@ __device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int i
     q0 = j_lo / BN;
     q1 = j_hi > j_lo ? (j_hi + BN - 1) / BN : q0;
   }
-  const long long T = t.Tc + Tp;
-  const int r0 = static_cast<int>(T * split / p.splits);
-  const int r1 = static_cast<int>(T * (split + 1) / p.splits);
-  t.cb = max(c0, r0);
-  t.ce = max(t.cb, min(c1, r1));
-  t.pb = max(t.Tc + q0, r0);
-  t.pe = max(t.pb, min(t.Tc + q1, r1));
+  const int lo = static_cast<int>(r0 < 0 ? 0 : r0);
+  const int hi = static_cast<int>(r1 > (1LL << 30) ? (1LL << 30) : r1);
+  t.cb = max(c0, lo);
+  t.ce = max(t.cb, min(c1, hi));
+  t.pb = max(t.Tc + q0, lo);
+  t.pe = max(t.pb, min(t.Tc + q1, hi));
   return t;
+}
+
+// Live key tiles of split `split` (of p.splits): split s owns [s*T/S, (s+1)*T/S).
+template <int BN>
+__device__ __forceinline__ TilePlan plan_tiles(const AttnParams& p, int b, int i_min, int i_max, int split) {
+  const long long T = (p.C + BN - 1) / BN + (p.P + BN - 1) / BN;
+  return plan_tiles_range<BN>(p, b, i_min, i_max, T * split / p.splits, T * (split + 1) / p.splits);
+}
+
+// All live key tiles of query rows [i_min, i_max] of sequence b.
+template <int BN>
+__device__ __forceinline__ TilePlan plan_whole(const AttnParams& p, int b, int i_min, int i_max) {
+  return plan_tiles_range<BN>(p, b, i_min, i_max, 0, 1LL << 30);
 }
 
 // Visible key interval of query row i, relative to a tile's first key
