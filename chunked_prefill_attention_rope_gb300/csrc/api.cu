@@ -56,7 +56,8 @@ int num_sms() {
 enum Path { kPathSingle = 0, kPathPair = 1, kPathDecode = 2 };
 
 struct Geometry {
-  int G, R, nq, splits, path, ctas;
+  int G, R, nq, splits, path;
+  PairTeams teams;
 };
 
 // Kernel path and work split for these sizes.  The host cannot see per-sequence
@@ -72,12 +73,12 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   g.G = Hq / Hkv;
   g.R = 128 / g.G;
   g.nq = (C + g.R - 1) / g.R;
-  g.ctas = 0;
+  g.teams = PairTeams{};
   const int sms = num_sms();
   if (attn_uses_pair(D, g.nq) && !attn_uses_decode(D, C, g.G)) {
     g.path = kPathPair;
     g.splits = 1;
-    g.ctas = pair_ctas(B, Hkv, g.nq, P, C, sms);
+    g.teams = pair_teams(B, Hkv, g.nq, P, C, sms);
     return g;
   }
   g.path = attn_uses_decode(D, C, g.G) ? kPathDecode : kPathSingle;
@@ -92,7 +93,7 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
 }
 
 size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
-  if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, g.nq, D, C, g.ctas).total;
+  if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, D, C, g.teams).total;
   if (g.splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * C;
   const size_t o = static_cast<size_t>(g.splits) * rows * D * sizeof(float);
@@ -192,11 +193,16 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   p.err = a->err;
   p.k_new = static_cast<const uint16_t*>(a->k_new);
   if (g.path == kPathPair) {
-    p.pairs = (g.nq + 1) / 2;
-    p.units = a->B * a->Hkv * p.pairs;
-    p.ctas = g.ctas;
+    const PairTeams& t = g.teams;
+    p.pairs = t.pairs;
+    p.units = a->B * a->Hkv * t.pairs;
+    p.team = t.team;
+    p.nblk = t.nblk;
+    p.blocks = t.blocks;
+    p.teams = t.teams;
+    p.ctas = t.ctas;
     uint8_t* w = static_cast<uint8_t*>(a->workspace);
-    const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, g.nq, a->D, a->C, g.ctas);
+    const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, a->D, a->C, t);
     p.ustart = reinterpret_cast<int32_t*>(w + L.ustart);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
     p.part_lse = reinterpret_cast<float*>(w + L.part_lse);

@@ -7,12 +7,17 @@
 //
 //   * Work unit = 256 packed query rows of one (sequence, kv head): query tiles
 //     Q0 and Q1 of 128 rows that share every K/V tile.
-//   * plan_units_kernel counts the live key tiles of every unit (lengths live
-//     on the device) and prefix-sums them.  The persistent CTAs then split the
-//     concatenated tile sequence into equal contiguous ranges (stream-K): a CTA
-//     finishes whole units directly and writes partial results only for the at
-//     most two units cut at its range ends; merge_units_kernel combines those
-//     in fixed order and zero-fills units without live keys.
+//   * Team-aligned stream-K.  The CTAs form teams of `team` CTAs; member m
+//     of a team handles pair blk*team + m of each block of pairs of one
+//     (sequence, kv head).  plan_units_kernel counts the live key tiles of
+//     every block (lengths live on the device) and prefix-sums them with a
+//     unit-switch cost.  Each team takes an equal contiguous range of that
+//     sequence; its members walk the same key tiles of the same block in
+//     lockstep, so every K/V tile a team loads is shared through L2 by all
+//     the pairs of the block.  A member finishes whole units directly and
+//     writes partial results only for the units cut at its team's range ends;
+//     merge_units_kernel combines those in fixed order and zero-fills units
+//     without live keys.
 //   * RoPE: rope_prep_kernel rotates the chunk's queries and keys once per call
 //     (coalesced, the same fp32 rounding as the cache append) into the
 //     workspace; the attention kernel TMA-loads rotated Q tiles and chunk-K
@@ -75,6 +80,26 @@ struct Unit {
   int b, kvh, pair;
 };
 
+// Block g = (b, kvh, blk): pairs [blk*team, (blk+1)*team) of one (sequence, kv head).
+struct Block {
+  int b, kvh, blk;
+};
+
+__device__ __forceinline__ Block block_of(const AttnParams& p, int g) {
+  Block x;
+  x.blk = g % p.nblk;
+  x.kvh = (g / p.nblk) % p.Hkv;
+  x.b = g / (p.nblk * p.Hkv);
+  return x;
+}
+
+// Live key tiles of all rows of a block: the tiles its members walk together.
+__device__ __forceinline__ TilePlan block_plan(const AttnParams& p, const Block& x) {
+  const int i_min = x.blk * p.team * 2 * p.R;
+  const int i_max = min(i_min + p.team * 2 * p.R, p.C) - 1;
+  return plan_whole<kBN>(p, x.b, i_min, i_max);
+}
+
 __device__ __forceinline__ Unit unit_of(const AttnParams& p, int u) {
   Unit x;
   x.pair = u % p.pairs;
@@ -83,10 +108,8 @@ __device__ __forceinline__ Unit unit_of(const AttnParams& p, int u) {
   return x;
 }
 
-__device__ __forceinline__ TilePlan unit_plan(const AttnParams& p, const Unit& x) {
-  const int i_min = x.pair * 2 * p.R;
-  const int i_max = min(i_min + 2 * p.R, p.C) - 1;
-  return plan_whole<kBN>(p, x.b, i_min, i_max);
+__device__ __forceinline__ int unit_id(const AttnParams& p, int b, int kvh, int pair) {
+  return (b * p.Hkv + kvh) * p.pairs + pair;
 }
 
 // First tile of CTA c's range in the concatenated tile sequence of T tiles.
@@ -103,35 +126,42 @@ __device__ __forceinline__ int unit_at(const int32_t* start, int U, long long x)
   return lo;
 }
 
-// Walks the (unit, first tile, end tile) segments of CTA c's range of cost
-// positions.
+// Walks the (block, first tile, end tile) segments of a team's range of cost
+// positions, for one member: segments whose pair does not exist are skipped.
 struct SegWalk {
   const int32_t* start;
-  int U, u;
+  int NB, g, member;
   long long lo, hi;
-  __device__ __forceinline__ void init(const AttnParams& p, int c) {
+  const AttnParams* pp;
+  __device__ __forceinline__ void init(const AttnParams& p, int cta) {
+    pp = &p;
     start = p.ustart;
-    U = p.units;
-    const long long T = start[U];
-    lo = cta_lo(T, c, p.ctas);
-    hi = cta_lo(T, c + 1, p.ctas);
-    u = lo < hi ? unit_at(start, U, lo) : U;
+    NB = p.blocks;
+    member = cta % p.team;
+    const int t = cta / p.team;
+    const long long T = start[NB];
+    lo = cta_lo(T, t, p.teams);
+    hi = cta_lo(T, t + 1, p.teams);
+    g = lo < hi ? unit_at(start, NB, lo) : NB;
   }
-  // Next segment holding at least one key tile; false when the range is
-  // exhausted.  Unit u spans cost positions [start[u], start[u+1]): first the
-  // switch cost, then one position per key tile.
-  __device__ __forceinline__ bool next(int& unit, int& a, int& e) {
-    while (u < U && start[u] < hi) {
-      const long long t0 = start[u] + kSwitchCost, s1 = start[u + 1];
-      const int cur = u++;
+  // Next segment holding at least one key tile of this member's unit; false
+  // when the range is exhausted.  Block g spans cost positions
+  // [start[g], start[g+1]): first the switch cost, then one per key tile.
+  __device__ __forceinline__ bool next(int& unit, Block& blk, int& a, int& e) {
+    while (g < NB && start[g] < hi) {
+      const long long t0 = start[g] + kSwitchCost, s1 = start[g + 1];
+      const int cur = g++;
       const long long aa = lo > t0 ? lo : t0;
       const long long ee = hi < s1 ? hi : s1;
-      if (ee > aa) {
-        unit = cur;
-        a = static_cast<int>(aa - t0);
-        e = static_cast<int>(ee - t0);
-        return true;
-      }
+      if (ee <= aa) continue;
+      const Block x = block_of(*pp, cur);
+      const int pair = x.blk * pp->team + member;
+      if (pair >= pp->pairs) continue;
+      blk = x;
+      unit = unit_id(*pp, x.b, x.kvh, pair);
+      a = static_cast<int>(aa - t0);
+      e = static_cast<int>(ee - t0);
+      return true;
     }
     return false;
   }
@@ -167,7 +197,7 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const AttnParams p) {
   }
 }
 
-// Cost of every unit (its live key tiles plus the switch cost) and the
+// Cost of every block (its live key tiles plus the switch cost) and the
 // exclusive prefix sum of the costs (one CTA).
 __global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
   __shared__ int32_t warp_sums[32];
@@ -175,11 +205,11 @@ __global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  for (int base = 0; base < p.units; base += 1024) {
+  for (int base = 0; base < p.blocks; base += 1024) {
     const int u = base + threadIdx.x;
     int n = 0;
-    if (u < p.units) {
-      n = unit_plan(p, unit_of(p, u)).count();
+    if (u < p.blocks) {
+      n = block_plan(p, block_of(p, u)).count();
       if (n > 0) n += kSwitchCost;
     }
     int incl = n;  // inclusive scan within the warp
@@ -201,12 +231,12 @@ __global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
     }
     __syncthreads();
     const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    if (u < p.units) p.ustart[u] = before + incl - n;
+    if (u < p.blocks) p.ustart[u] = before + incl - n;
     __syncthreads();
     if (threadIdx.x == 1023) carry = before + incl;
     __syncthreads();
   }
-  if (threadIdx.x == 0) p.ustart[p.units] = carry;
+  if (threadIdx.x == 0) p.ustart[p.blocks] = carry;
 }
 
 template <int D, bool EXPLICIT>
@@ -272,9 +302,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       int g = 0;  // tiles issued (chunk keys come from the rotated copy behind map_kn)
       bool ok = true;
       int unit, a, e;
-      while (ok && walk.next(unit, a, e)) {
+      Block bx;
+      while (ok && walk.next(unit, bx, a, e)) {
         const Unit x = unit_of(p, unit);
-        const TilePlan tp = unit_plan(p, x);
+        const TilePlan tp = block_plan(p, bx);
         for (int j = a; j < e; ++j, ++g) {
           const int st = g % NS;
           if (!(ok = mbar_wait(&bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
@@ -331,8 +362,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
       };
       int unit, a, e;
-      while (ok && walk.next(unit, a, e)) {
-        const TilePlan tp = unit_plan(p, unit_of(p, unit));
+      Block bx;
+      while (ok && walk.next(unit, bx, a, e)) {
+        const TilePlan tp = block_plan(p, bx);
         const int n = e - a;
         if (!(ok = k_ready(tp, a, g) && mbar_wait(&bars->q_full[0], seg & 1, abort))) break;
         tc_fence_after();
@@ -377,7 +409,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       int seg = 0;
       bool ok = true;
       int unit, a, e;
-      while (ok && walk.next(unit, a, e)) {
+      Block bx;
+      while (ok && walk.next(unit, bx, a, e)) {
         const Unit x = unit_of(p, unit);
         for (int qi = 0; qi < 2 && ok; ++qi) {
           // the previous segment's S = Q K products of this tile have completed
@@ -407,9 +440,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     int g = 0, seg = 0;
     bool ok = true;
     int unit, a, e;
-    while (ok && walk.next(unit, a, e)) {
+    Block bx;
+    while (ok && walk.next(unit, bx, a, e)) {
       const Unit x = unit_of(p, unit);
-      const TilePlan tp = unit_plan(p, x);
+      const TilePlan tp = block_plan(p, bx);
       const int qt = x.pair * 2 + qi;
       const int gr = row / p.R;
       const int i = qt * p.R + row % p.R;
@@ -603,23 +637,28 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 }
 
 // Final rows of units cut between CTAs (merged in CTA order) and of units with
-// no live key tile (zeros).  One CTA per unit; whole units exit at once.
+// no live key tile (zeros).  CTA (unit, group) handles 32 of the unit's 256
+// rows, one per warp; units finished by a single CTA exit at once.
 constexpr int kMaxCtas = 256;
 
 __global__ void __launch_bounds__(1024) merge_units_kernel(const AttnParams p) {
   __shared__ int piece_slot[kMaxCtas];  // partial-result slot of each piece, in CTA order
   __shared__ int n_pieces;
   const int unit = blockIdx.x;
-  const long long s0 = p.ustart[unit], s1 = p.ustart[unit + 1];
-  const long long T = p.ustart[p.units];
+  const Unit ux = unit_of(p, unit);
+  const int gblk = (ux.b * p.Hkv + ux.kvh) * p.nblk + ux.pair / p.team;
+  const int member = ux.pair % p.team;
+  const long long s0 = p.ustart[gblk], s1 = p.ustart[gblk + 1];
+  const long long T = p.ustart[p.blocks];
   if (threadIdx.x == 0) {
-    // CTA c covers cost positions [floor(c T / ctas), floor((c+1) T / ctas));
-    // the last CTA whose range starts at or before x is floor(((x + 1) ctas - 1) / T).
+    // team t covers cost positions [floor(t T / teams), floor((t+1) T / teams));
+    // the last team whose range starts at or before x is floor(((x + 1) teams - 1) / T).
     int np = 0;
     if (s1 > s0) {
-      const int c_first = static_cast<int>(((s0 + 1) * p.ctas - 1) / T);
-      const int c_last = static_cast<int>((s1 * p.ctas - 1) / T);
-      for (int c = c_first; c <= c_last; ++c) {
+      const int t_first = static_cast<int>(((s0 + 1) * p.teams - 1) / T);
+      const int t_last = static_cast<int>((s1 * p.teams - 1) / T);
+      for (int t = t_first; t <= t_last; ++t) {
+        const int c = t * p.team + member;
         if (p.ptag[2 * c] == unit) piece_slot[np++] = 2 * c;
         else if (p.ptag[2 * c + 1] == unit) piece_slot[np++] = 2 * c + 1;
       }
@@ -630,17 +669,18 @@ __global__ void __launch_bounds__(1024) merge_units_kernel(const AttnParams p) {
   __syncthreads();
   const int np = n_pieces;
   if (np < 0) return;
-  const Unit x = unit_of(p, unit);
+  const Unit x = ux;
   const int D = p.D;
   const int n_real = p.n_real ? min(max(p.n_real[x.b], 0), p.C) : p.C;
   const int sel = p.sel_row ? p.sel_row[x.b] : n_real - 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per = D / 32;
-  for (int r = warp; r < kUnitRows; r += 32) {
+  {
+    const int r = blockIdx.y * 32 + warp;
     const int qi = r / 128, rr = r % 128;
     const int gr = rr / p.R;
     const int i = (x.pair * 2 + qi) * p.R + rr % p.R;
-    if (gr >= p.G || i >= p.C) continue;
+    if (gr >= p.G || i >= p.C) return;
     const int h = x.kvh * p.G + gr;
     const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h) * p.C + i;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -677,19 +717,26 @@ __global__ void __launch_bounds__(1024) merge_units_kernel(const AttnParams p) {
   }
 }
 
-int pair_ctas(int B, int Hkv, int nq, int P, int C, int num_sms) {
-  const long long units = static_cast<long long>(B) * Hkv * ((nq + 1) / 2);
-  const long long max_tiles = units * ((P + kBN - 1) / kBN + (C + kBN - 1) / kBN);
-  const long long cap = num_sms < kMaxCtas ? num_sms : kMaxCtas;
-  return static_cast<int>(max(1LL, min(cap, max_tiles)));
+PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms) {
+  PairTeams t;
+  t.pairs = (nq + 1) / 2;
+  const int sms = num_sms < kMaxCtas ? num_sms : kMaxCtas;
+  t.team = t.pairs < sms ? t.pairs : sms;
+  t.nblk = (t.pairs + t.team - 1) / t.team;
+  t.blocks = B * Hkv * t.nblk;
+  const long long max_cost = static_cast<long long>(t.blocks) *
+                             ((P + kBN - 1) / kBN + (C + kBN - 1) / kBN + kSwitchCost);
+  t.teams = static_cast<int>(max(1LL, min(static_cast<long long>(sms / t.team), max_cost)));
+  t.ctas = t.teams * t.team;
+  return t;
 }
 
-PairWorkspace pair_workspace(int B, int Hq, int Hkv, int nq, int D, int C, int ctas) {
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t units = static_cast<size_t>(B) * Hkv * ((nq + 1) / 2);
+  const int ctas = t.ctas;
   PairWorkspace w;
   size_t off = 0;
-  w.ustart = off; off += al((units + 1) * sizeof(int32_t));
+  w.ustart = off; off += al((static_cast<size_t>(t.blocks) + 1) * sizeof(int32_t));
   w.part_o = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * D * sizeof(float));
   w.part_lse = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * sizeof(float));
   w.ptag = off; off += al(static_cast<size_t>(ctas) * 2 * sizeof(int32_t));
@@ -714,7 +761,7 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
   rope_prep_kernel<<<blocks, 256, 0, stream>>>(p);
   plan_units_kernel<<<1, 1024, 0, stream>>>(p);
   kern<<<p.ctas, kThreadsPair, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  merge_units_kernel<<<p.units, 1024, 0, stream>>>(p);
+  merge_units_kernel<<<dim3(p.units, kUnitRows / 32), 1024, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -23,23 +23,30 @@ struct AttnParams {
   float* part_o;    // split-KV partials [splits][B][Hq][C][D] or null
   float* part_lse;  // [splits][B][Hq][C]
   int32_t* err;
-  // persistent stream-K path (two query tiles per work unit)
-  int32_t* ustart;  // [units + 1] exclusive prefix sum of live tiles per unit
+  // persistent team-aligned stream-K path (two query tiles per work unit)
+  int32_t* ustart;  // [blocks + 1] exclusive prefix sum of block costs
   int units;        // B * Hkv * pairs
   int pairs;        // query-tile pairs per (sequence, kv head)
-  int ctas;         // persistent CTAs
+  int team;         // CTAs per team = pairs per block
+  int nblk;         // blocks per (sequence, kv head)
+  int blocks;       // B * Hkv * nblk
+  int teams;        // teams of CTAs
+  int ctas;         // persistent CTAs = teams * team
   const uint16_t* k_new;  // chunk keys before RoPE [B, Hkv, C, D]
   uint16_t* q_rot;        // rotated queries [B, Hq, C, D] (workspace)
   uint16_t* k_rot;        // rotated chunk keys [B, Hkv, C, D] (workspace)
   int32_t* ptag;          // [2 * ctas] unit of each CTA's partial slots (-1: none)
 };
 
-// Persistent stream-K layout: number of CTAs and workspace bytes for these sizes.
-int pair_ctas(int B, int Hkv, int nq, int P, int C, int num_sms);
+// Team-aligned stream-K layout for these sizes, and its workspace.
+struct PairTeams {
+  int pairs, team, nblk, blocks, teams, ctas;
+};
+PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms);
 struct PairWorkspace {
   size_t ustart, part_o, part_lse, ptag, q_rot, k_rot, total;
 };
-PairWorkspace pair_workspace(int B, int Hq, int Hkv, int nq, int D, int C, int ctas);
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t);
 // maps for the pair path: cache K, cache V, rotated chunk K, chunk V, rotated Q
 // (dims {D, C, Hq, B}, box {64, R, G, 1}).
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
