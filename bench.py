@@ -39,6 +39,39 @@ from synth import WORKLOADS, make_chunk_inputs, make_cache  # noqa: E402
 
 METRIC = "chunk-prefill attn tokens/s & TFLOP/s (% bf16 peak); decode KV-read GB/s"
 
+# DRAM bytes (read + write) per call of the dominant kernels, from one ncu
+# capture of the same workload, valid only for the kernel sources they were
+# measured on (sha256 over those files); anything else reports null.
+KERNEL_SOURCES = {
+    "prefill": ["attn_pair.cu", "tiles.cuh", "common.cuh", "kernels.h"],
+    "decode": ["decode.cu", "tiles.cuh", "common.cuh", "kernels.h"],
+}
+MEASURED_TRAFFIC = {}
+
+
+def source_hash(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "chunked_prefill_attention_rope_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kind):
+    rec = MEASURED_TRAFFIC.get(kind)
+    return rec["bytes"] if rec and rec["src"] == source_hash(kind) else None
+
+
+def attn_launches(w, workspace_bytes):
+    """Kernel launches of one attention call (mirrors the library's path choice)."""
+    G = w.Hq // w.Hkv
+    nq = -(-w.C // (128 // G))
+    decode = w.C == 1 and w.D in (64, 128) and G <= 16
+    if w.D in (64, 128) and nq >= 2 and not decode:
+        return 4          # RoPE pre-pass, plan, attention, merge
+    return 1 + (workspace_bytes > 0)
+
 
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -134,7 +167,7 @@ def setup_parts(cpa, dev):
     p.cache = cpa.KVCache(ck, cv, p.len0.clone())
     p.out = torch.empty((w.B, w.Hq, w.C, w.D), dtype=torch.bfloat16, device=dev)
     p.ws = torch.empty(max(1, cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)), dtype=torch.uint8, device=dev)
-    p.launches = 1 + (cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P) > 0) + 2
+    p.launches = attn_launches(w, cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)) + 2
     p.flops, p.bytes = prefill_work(w, p.len0.cpu().numpy())
     p.tokens = int(p.inp["n_real"].sum())
     parts["prefill"] = p
@@ -149,7 +182,7 @@ def setup_parts(cpa, dev):
     d.out = torch.empty((w.B, w.Hq, 1, w.D), dtype=torch.bfloat16, device=dev)
     need = cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, 1, w.P)
     d.ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
-    d.launches = 1 + (need > 0) + 2
+    d.launches = attn_launches(w, need) + 2
     L = d.len0.cpu().numpy().astype(np.int64)
     d.flops = int(4 * w.D * w.Hq * (L + 1).sum())
     d.kv_bytes = int(L.sum()) * w.Hkv * w.D * 2 * 2
@@ -169,7 +202,7 @@ def setup_parts(cpa, dev):
     t.out = torch.empty((w.B, w.Hq, w.C, w.D), dtype=torch.bfloat16, device=dev)
     need = cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)
     t.ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
-    t.launches = 1 + 1 + (need > 0) + 2 + 2
+    t.launches = 1 + attn_launches(w, need) + 2 + 2
     t.tokens = int(t.inp["n_real"].sum())
     parts["tail"] = t
     return parts
@@ -291,13 +324,17 @@ def ours(args, rank, world, dev):
     dc_gbs = dc.bytes / (t_dc * 1e-3) / 1e9
     # roofline of the dominant kernel (longest CUDA-event time in the step)
     if t_pf >= t_dc:
+        tr = traffic_for("prefill")
         roof = {"bound": "tensor", "achieved": round(pf_tflops, 1), "peak": tf_burst, "unit": "TFLOP/s",
-                "frac": round(pf_tflops / tf_burst, 4), "traffic": None,
-                "kernel": "attn_pair_kernel<128,false> (long-context chunk attention)",
+                "frac": round(pf_tflops / tf_burst, 4), "traffic": tr,
+                "algorithmic_bytes": pf.bytes,
+                "kernel": "chunk_prefill_attn on the long-context chunk (RoPE pre-pass + plan + "
+                          "attn_pair_kernel<128,false> + merge)",
                 "peak_source": f"{src} burst bf16 (MEASURED_PEAKS.json)"}
     else:
         roof = {"bound": "hbm", "achieved": round(dc_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(dc_gbs / hbm, 4), "traffic": None,
+                "frac": round(dc_gbs / hbm, 4), "traffic": traffic_for("decode"),
+                "algorithmic_bytes": dc.bytes,
                 "kernel": "attn_decode_kernel<128,false> (decode attention)",
                 "peak_source": f"{src} HBM copy (MEASURED_PEAKS.json)"}
     line = {

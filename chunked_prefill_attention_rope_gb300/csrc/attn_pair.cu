@@ -33,7 +33,8 @@
 //     multiply-add per two scores (masked scores are -inf and give exactly 0).
 //
 // Warps: 0-3 softmax for Q0, 4-7 softmax for Q1 (warp w owns TMEM lanes
-// 32*(w%4)..+31), 8 K/V TMA producer, 9 MMA issuer, 10 Q TMA loader.  Every
+// 32*(w%4)..+31), 8 K/V TMA producer, 9 MMA issuer, 10 Q TMA loader, 11 idle
+// (it completes the aux warpgroup for the register split).  Every
 // role walks the same segment sequence and counts tiles globally, so barrier
 // phases carry across unit boundaries.
 #include "tiles.cuh"
@@ -43,7 +44,13 @@ namespace cpa {
 namespace {
 
 constexpr int kBN = 128;
-constexpr int kThreadsPair = 352;
+constexpr int kThreadsPair = 384;
+// Register split (setmaxnreg): the launch gives every thread 168 registers
+// (384 x 168 = 64512).  The aux warpgroup (warps 8-11) drops to 96, freeing
+// 128 x 72 = 9216; the two softmax warpgroups rise to 200, taking
+// 2 x 128 x 32 = 8192 <= 9216, so the increase never waits on the pool.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsAux = 96;
 constexpr int kUnitRows = 256;
 // A unit switch (Q reload, epilogue, pipeline refill) costs about this many key
 // tiles; the stream-K split charges it to every non-empty unit.
@@ -292,6 +299,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   SegWalk walk;
   walk.init(p, cta);
 
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsAux));
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -429,7 +438,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         while (!mbar_try_wait(&bars->q_full[qi], (seg - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
     }
+  }  // warp 11: no role
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax (query tile qi)
     const int qi = warp / 4;
     const int row = 32 * (warp & 3) + lane;
