@@ -46,7 +46,12 @@ KERNEL_SOURCES = {
     "prefill": ["attn_pair.cu", "tiles.cuh", "common.cuh", "kernels.h"],
     "decode": ["decode.cu", "tiles.cuh", "common.cuh", "kernels.h"],
 }
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # long-context chunk call: rope_prep + plan + attn_pair + merge (profiles/dram_traffic_calls.md)
+    "prefill": {"src": "46b30b7784a8c7e9", "bytes": 657603840},
+    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0085 x)
+    "decode": {"src": "ed4fceee0fa400aa", "bytes": 4836855406},
+}
 
 
 def source_hash(kind):
