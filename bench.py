@@ -463,6 +463,34 @@ def reference(args, rank, world):
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(name, reps, batch=None):
+    """Run one workload's attention call `reps` times on cuda:0 (for profiler
+    captures: the n-th launch of a kernel is the n-th call)."""
+    import dataclasses
+    import chunked_prefill_attention_rope_gb300 as cpa
+    from chunked_prefill_attention_rope_gb300.build import build
+    build()
+    w = WORKLOADS[name]
+    if batch:
+        w = dataclasses.replace(w, B=batch)
+    dev = torch.device("cuda", 0)
+    inp = make_chunk_inputs(w, device=dev)
+    ck, cv = make_cache(w, device=dev)
+    cache = cpa.KVCache(ck, cv, inp["past_len"].clone())
+    out = torch.empty((w.B, w.Hq, w.C, w.D), dtype=torch.bfloat16, device=dev)
+    need = cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)
+    ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+    err = cpa.new_error_word(dev)
+    f = cpa.decode_step if w.C == 1 else cpa.chunk_prefill_attn
+    for _ in range(reps):
+        f(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], cache, w.P, past_len=inp["past_len"],
+          n_real=inp["n_real"], window=w.window, causal=bool(w.causal), out=out, workspace=ws, err=err)
+    torch.cuda.synchronize()
+    if int(err[0]) != 0:
+        raise RuntimeError(f"device error bits {int(err[0])}")
+    print(json.dumps({"case": name, "B": w.B, "reps": reps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,7 +499,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--case", default=None, help="run only this workload's attention call (profiling)")
+    ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=None)
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.reps, args.batch)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
