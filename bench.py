@@ -74,7 +74,7 @@ def attn_launches(w, workspace_bytes):
     nq = -(-w.C // (128 // G))
     decode = w.C == 1 and w.D in (64, 128) and G <= 16
     if w.D in (64, 128) and nq >= 2 and not decode:
-        return 4          # RoPE pre-pass, plan, attention, merge
+        return 3          # RoPE pre-pass with the plan, attention, merge
     return 1 + (workspace_bytes > 0)
 
 

@@ -209,24 +209,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = g < p.G && i < p.C;
     const int h = kvh * p.G + (valid ? g : 0);
 
-    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.
-    for (int item = tid; item < kBM * (D / 16); item += 128) {
-      const int r = item / (D / 16);
-      const int kc = item % (D / 16);
-      const int rg = r / p.R;
-      const int ri = qt * p.R + r % p.R;
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (rg < p.G && ri < p.C) {
-        const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + rg) * p.C + ri) * D;
-        lo = *reinterpret_cast<const uint4*>(p.q + rowoff + kc * 8);
-        hi = *reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc * 8);
-        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-        rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.  The
+    // G heads of chunk row i share its table row: each item loads the tables
+    // of one (row, chunk pair) once and rotates that pair for every head, the
+    // loads of four heads issued together.
+    {
+      const int R = p.R;
+      for (int item = tid; item < R * (D / 16); item += 128) {
+        const int il = item / (D / 16);
+        const int kc = item % (D / 16);
+        const int kh = kc + D / 16;
+        const int ri = qt * R + il;
+        const bool in = ri < p.C;
+        RopeTab tab{};
+        if (in) {
+          const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
+          const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
+          tab = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+        }
+        for (int g0 = 0; g0 < p.G; g0 += 4) {
+          uint4 lo[4], hi[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            lo[u] = make_uint4(0, 0, 0, 0);
+            hi[u] = lo[u];
+            const int g = g0 + u;
+            if (in && g < p.G) {
+              const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.C + ri) * D;
+              lo[u] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + kc * 8));
+              hi[u] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc * 8));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int g = g0 + u;
+            if (g >= p.G) break;
+            if (in) rope_apply(lo[u], hi[u], tab);
+            const int r = g * R + il;
+            *reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8)) = lo[u];
+            *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi[u];
+          }
+        }
       }
-      const int kh = kc + D / 16;
-      *reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8)) = lo;
-      *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi;
+      // rows past the G * R packed rows stay zero
+      for (int item = tid; item < (kBM - p.G * R) * (D / 8); item += 128) {
+        const int r = p.G * R + item / (D / 8);
+        const int c = item % (D / 8);
+        *reinterpret_cast<uint4*>(sQ + (c / 8) * (kBM * 128) + sw128(r, c % 8)) = make_uint4(0, 0, 0, 0);
+      }
     }
     fence_async_smem();
     mbar_arrive(&bars->q_ready);
@@ -252,20 +282,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rotate the raw chunk-K tile in place
         if (!(ok = warp_all(mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort)))) break;
         uint8_t* kt = sK + st * SM::kKBytes;
-        for (int item = tid; item < BN * (D / 16); item += 128) {
-          const int r = item / (D / 16);
-          const int kc = item % (D / 16);
-          const int t = base + r;
-          if (t >= p.C) continue;
-          const int kh = kc + D / 16;
-          uint4* plo = reinterpret_cast<uint4*>(kt + (kc / 8) * (BN * 128) + sw128(r, kc % 8));
-          uint4* phi = reinterpret_cast<uint4*>(kt + (kh / 8) * (BN * 128) + sw128(r, kh % 8));
-          uint4 lo = *plo, hi = *phi;
-          const float* cr = p.cos + (static_cast<size_t>(b) * p.C + t) * D;
-          const float* sr = p.sin + (static_cast<size_t>(b) * p.C + t) * D;
-          rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-          *plo = lo;
-          *phi = hi;
+        // KU items per step, their table loads issued together (one where
+        // the 128-key S tile leaves no registers for more)
+        constexpr int KU = BN == 64 ? 2 : 1;
+        for (int item0 = tid; item0 < BN * (D / 16); item0 += 128 * KU) {
+          RopeTab tab[KU];
+          uint4* pl[KU];
+          uint4* ph[KU];
+          bool use[KU];
+#pragma unroll
+          for (int u = 0; u < KU; ++u) {
+            const int item = item0 + 128 * u;
+            const int r = item / (D / 16);
+            const int kc = item % (D / 16);
+            const int t = base + r;
+            use[u] = item < BN * (D / 16) && t < p.C;
+            const int kh = kc + D / 16;
+            pl[u] = reinterpret_cast<uint4*>(kt + (kc / 8) * (BN * 128) + sw128(r, kc % 8));
+            ph[u] = reinterpret_cast<uint4*>(kt + (kh / 8) * (BN * 128) + sw128(r, kh % 8));
+            if (use[u]) {
+              const float* cr = p.cos + (static_cast<size_t>(b) * p.C + t) * D;
+              const float* sr = p.sin + (static_cast<size_t>(b) * p.C + t) * D;
+              tab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < KU; ++u) {
+            if (!use[u]) continue;
+            uint4 lo = *pl[u], hi = *ph[u];
+            rope_apply(lo, hi, tab[u]);
+            *pl[u] = lo;
+            *ph[u] = hi;
+          }
         }
         fence_async_smem();
         mbar_arrive(&bars->k_rot[st]);

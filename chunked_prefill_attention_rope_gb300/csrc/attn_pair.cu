@@ -9,7 +9,7 @@
 //     Q0 and Q1 of 128 rows that share every K/V tile.
 //   * Team-aligned stream-K.  The CTAs form teams of `team` CTAs; member m
 //     of a team handles pair blk*team + m of each block of pairs of one
-//     (sequence, kv head).  plan_units_kernel counts the live key tiles of
+//     (sequence, kv head).  The planning CTA of prep_kernel counts the live key tiles of
 //     every block (lengths live on the device) and prefix-sums them with a
 //     unit-switch cost.  Each team takes an equal contiguous range of that
 //     sequence; its members walk the same key tiles of the same block in
@@ -18,7 +18,7 @@
 //     writes partial results only for the units cut at its team's range ends;
 //     merge_units_kernel combines those in fixed order and zero-fills units
 //     without live keys.
-//   * RoPE: rope_prep_kernel rotates the chunk's queries and keys once per call
+//   * RoPE: prep_kernel rotates the chunk's queries and keys once per call
 //     (coalesced, the same fp32 rounding as the cache append) into the
 //     workspace; the attention kernel TMA-loads rotated Q tiles and chunk-K
 //     tiles from there, so no tile is rotated twice and no load waits on a
@@ -37,6 +37,8 @@
 // (it completes the aux warpgroup for the register split).  Every
 // role walks the same segment sequence and counts tiles globally, so barrier
 // phases carry across unit boundaries.
+#include <type_traits>
+
 #include "tiles.cuh"
 
 namespace cpa {
@@ -176,43 +178,19 @@ struct SegWalk {
 
 }  // namespace
 
-// Rotated copies of the chunk's queries and keys (RoPE from the per-row
-// cos/sin tables, fp32 products and sums without fused multiply-add, bf16
-// round-to-nearest-even: the bytes the cache append writes for K).
-__global__ void __launch_bounds__(256) rope_prep_kernel(const AttnParams p) {
-  const int D = p.D;
-  const int HP = D / 16;  // 8-element chunk pairs (d, d + D/2) per row
-  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.C;
-  const long long total = (rows_q + static_cast<long long>(p.B) * p.Hkv * p.C) * HP;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int kc = static_cast<int>(it % HP);
-    const long long row = it / HP;  // q rows first, then chunk-key rows
-    const bool is_q = row < rows_q;
-    const long long r = is_q ? row : row - rows_q;
-    const int i = static_cast<int>(r % p.C);
-    const int b = static_cast<int>(r / p.C / (is_q ? p.Hq : p.Hkv));
-    const uint16_t* src = (is_q ? p.q : p.k_new) + r * D;
-    uint16_t* dst = (is_q ? p.q_rot : p.k_rot) + r * D;
-    uint4 lo = *reinterpret_cast<const uint4*>(src + kc * 8);
-    uint4 hi = *reinterpret_cast<const uint4*>(src + D / 2 + kc * 8);
-    const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
-    const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
-    rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-    *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
-    *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
-  }
-}
+constexpr int kPrepThreads = 256;
+constexpr int kPrepHeads = 8;  // heads rotated per item with one table load
 
 // Cost of every block (its live key tiles plus the switch cost) and the
-// exclusive prefix sum of the costs (one CTA).
-__global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
-  __shared__ int32_t warp_sums[32];
+// exclusive prefix sum of the costs, by one CTA of kPrepThreads threads.
+__device__ void plan_units(const AttnParams& p) {
+  __shared__ int32_t warp_sums[kPrepThreads / 32];
   __shared__ int32_t carry;
+  constexpr int kWarps = kPrepThreads / 32;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  for (int base = 0; base < p.blocks; base += 1024) {
+  for (int base = 0; base < p.blocks; base += kPrepThreads) {
     const int u = base + threadIdx.x;
     int n = 0;
     if (u < p.blocks) {
@@ -228,22 +206,74 @@ __global__ void __launch_bounds__(1024) plan_units_kernel(const AttnParams p) {
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      int w = warp_sums[lane];
+      int w = lane < kWarps ? warp_sums[lane] : 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
+      for (int o = 1; o < kWarps; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, w, o);
         if (lane >= o) w += v;
       }
-      warp_sums[lane] = w;  // inclusive over warps
+      if (lane < kWarps) warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
     const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
     if (u < p.blocks) p.ustart[u] = before + incl - n;
     __syncthreads();
-    if (threadIdx.x == 1023) carry = before + incl;
+    if (threadIdx.x == kPrepThreads - 1) carry = before + incl;
     __syncthreads();
   }
   if (threadIdx.x == 0) p.ustart[p.blocks] = carry;
+}
+
+// The last CTA plans (plan_units); the others rotate the chunk's queries and
+// keys into the workspace.  An item is one (sequence, chunk row, chunk pair)
+// and up to eight heads of the combined list [query heads, key heads]: the
+// table values of its row are loaded once and the eight heads' loads are
+// issued together.  A warp covers four consecutive rows of each head, so
+// every load and store is a contiguous 512-byte run per head.
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) {
+  if (blockIdx.x == gridDim.x - 1) {
+    plan_units(p);
+    return;
+  }
+  const int D = p.D;
+  const int HP = D / 16;  // 8-element chunk pairs (d, d + D/2) per row
+  const int HH = p.Hq + p.Hkv;
+  const int groups = (HH + kPrepHeads - 1) / kPrepHeads;
+  const long long total = static_cast<long long>(p.B) * groups * p.C * HP;
+  const long long stride = static_cast<long long>(gridDim.x - 1) * blockDim.x;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total; it += stride) {
+    const int kc = static_cast<int>(it % HP);
+    long long t = it / HP;
+    const int i = static_cast<int>(t % p.C);
+    t /= p.C;
+    const int grp = static_cast<int>(t % groups);
+    const int b = static_cast<int>(t / groups);
+    const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
+    const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
+    const RopeTab tab = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    uint4 lo[kPrepHeads], hi[kPrepHeads];
+    size_t off[kPrepHeads];
+#pragma unroll
+    for (int u = 0; u < kPrepHeads; ++u) {
+      const int hh = grp * kPrepHeads + u;
+      if (hh >= HH) break;
+      const bool is_q = hh < p.Hq;
+      off[u] = is_q ? ((static_cast<size_t>(b) * p.Hq + hh) * p.C + i) * D
+                    : ((static_cast<size_t>(b) * p.Hkv + (hh - p.Hq)) * p.C + i) * D;
+      const uint16_t* src = (is_q ? p.q : p.k_new) + off[u];
+      lo[u] = __ldg(reinterpret_cast<const uint4*>(src + kc * 8));
+      hi[u] = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepHeads; ++u) {
+      const int hh = grp * kPrepHeads + u;
+      if (hh >= HH) break;
+      rope_apply(lo[u], hi[u], tab);
+      uint16_t* dst = (hh < p.Hq ? p.q_rot : p.k_rot) + off[u];
+      *reinterpret_cast<uint4*>(dst + kc * 8) = lo[u];
+      *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi[u];
+    }
+  }
 }
 
 template <int D, bool EXPLICIT>
@@ -652,74 +682,128 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 // rows, one per warp; units finished by a single CTA exit at once.
 constexpr int kMaxCtas = 256;
 
-__global__ void __launch_bounds__(1024) merge_units_kernel(const AttnParams p) {
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = 64;  // rows of one unit per merge block
+constexpr int kMergeRowBatch = 2;
+constexpr int kMergePieceBatch = 4;
+
+// One block per (unit, 64-row slab).  Warp 0 finds the unit's pieces (the
+// partial-result slots tagged with the unit, in CTA order) with one load per
+// lane; then each warp merges 8 rows, two rows and four pieces per batch with
+// all their loads issued before any use.  Pieces combine in CTA order with a
+// running maximum (one batch, and so the plain max-shifted weighted sum, when
+// a unit has at most four pieces).
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnParams p) {
   __shared__ int piece_slot[kMaxCtas];  // partial-result slot of each piece, in CTA order
   __shared__ int n_pieces;
+  constexpr int V = D / 32;  // floats per lane
+  using Vec = typename std::conditional<V == 4, float4, float2>::type;
   const int unit = blockIdx.x;
-  const Unit ux = unit_of(p, unit);
-  const int gblk = (ux.b * p.Hkv + ux.kvh) * p.nblk + ux.pair / p.team;
-  const int member = ux.pair % p.team;
-  const long long s0 = p.ustart[gblk], s1 = p.ustart[gblk + 1];
-  const long long T = p.ustart[p.blocks];
-  if (threadIdx.x == 0) {
-    // team t covers cost positions [floor(t T / teams), floor((t+1) T / teams));
-    // the last team whose range starts at or before x is floor(((x + 1) teams - 1) / T).
+  const Unit x = unit_of(p, unit);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) {
+    const int gblk = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
+    const int member = x.pair % p.team;
+    const long long s0 = p.ustart[gblk], s1 = p.ustart[gblk + 1];
+    const long long T = p.ustart[p.blocks];
     int np = 0;
     if (s1 > s0) {
+      // team t covers cost positions [floor(t T / teams), floor((t+1) T / teams));
+      // the last team whose range starts at or before x is floor(((x + 1) teams - 1) / T).
       const int t_first = static_cast<int>(((s0 + 1) * p.teams - 1) / T);
       const int t_last = static_cast<int>((s1 * p.teams - 1) / T);
-      for (int t = t_first; t <= t_last; ++t) {
-        const int c = t * p.team + member;
-        if (p.ptag[2 * c] == unit) piece_slot[np++] = 2 * c;
-        else if (p.ptag[2 * c + 1] == unit) piece_slot[np++] = 2 * c + 1;
+      for (int t0 = t_first; t0 <= t_last; t0 += 32) {
+        const int t = t0 + lane;
+        int slot = -1;
+        if (t <= t_last) {
+          const int c = t * p.team + member;
+          const int tag0 = p.ptag[2 * c], tag1 = p.ptag[2 * c + 1];
+          slot = tag0 == unit ? 2 * c : (tag1 == unit ? 2 * c + 1 : -1);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
+        if (slot >= 0) piece_slot[np + __popc(m & ((1u << lane) - 1u))] = slot;
+        np += __popc(m);
       }
       if (np == 0) np = -1;  // one CTA did the whole unit and wrote it already
     }
-    n_pieces = np;
+    if (lane == 0) n_pieces = np;
   }
   __syncthreads();
   const int np = n_pieces;
   if (np < 0) return;
-  const Unit x = ux;
-  const int D = p.D;
   const int n_real = p.n_real ? min(max(p.n_real[x.b], 0), p.C) : p.C;
   const int sel = p.sel_row ? p.sel_row[x.b] : n_real - 1;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int per = D / 32;
-  {
-    const int r = blockIdx.y * 32 + warp;
-    const int qi = r / 128, rr = r % 128;
-    const int gr = rr / p.R;
-    const int i = (x.pair * 2 + qi) * p.R + rr % p.R;
-    if (gr >= p.G || i >= p.C) return;
-    const int h = x.kvh * p.G + gr;
-    const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h) * p.C + i;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float lmax = -INFINITY;
-    for (int k = 0; k < np; ++k)
-      lmax = fmaxf(lmax, p.part_lse[static_cast<size_t>(piece_slot[k]) * kUnitRows + r]);
-    float wsum = 0.f;
-    if (lmax != -INFINITY) {
-      for (int k = 0; k < np; ++k) {
-        const size_t sidx = static_cast<size_t>(piece_slot[k]) * kUnitRows + r;
-        const float ls = p.part_lse[sidx];
-        if (ls == -INFINITY) continue;
-        const float w = fast_exp2(ls - lmax);
-        wsum += w;
-        const float* src = p.part_o + sidx * D + lane * per;
+  constexpr int kRowsPerWarp = kMergeRows / (kMergeThreads / 32);
+  for (int j0 = 0; j0 < kRowsPerWarp; j0 += kMergeRowBatch) {
+    int r[kMergeRowBatch], i[kMergeRowBatch], h[kMergeRowBatch];
+    bool live[kMergeRowBatch];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q < per) acc[q] = __fmaf_rn(w, src[q], acc[q]);
+    for (int u = 0; u < kMergeRowBatch; ++u) {
+      r[u] = blockIdx.y * kMergeRows + (j0 + u) * (kMergeThreads / 32) + warp;
+      const int qi = r[u] / 128, rr = r[u] % 128;
+      const int gr = rr / p.R;
+      i[u] = (x.pair * 2 + qi) * p.R + rr % p.R;
+      h[u] = x.kvh * p.G + gr;
+      live[u] = gr < p.G && i[u] < p.C;
+    }
+    float acc[kMergeRowBatch][V], m[kMergeRowBatch], wsum[kMergeRowBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeRowBatch; ++u) {
+      m[u] = -INFINITY;
+      wsum[u] = 0.f;
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
+    }
+    for (int k0 = 0; k0 < np; k0 += kMergePieceBatch) {
+      float ls[kMergeRowBatch][kMergePieceBatch];
+      Vec o[kMergeRowBatch][kMergePieceBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeRowBatch; ++u)
+#pragma unroll
+        for (int k = 0; k < kMergePieceBatch; ++k) {
+          ls[u][k] = -INFINITY;
+          if (live[u] && k0 + k < np) {
+            const size_t sidx = static_cast<size_t>(piece_slot[k0 + k]) * kUnitRows + r[u];
+            ls[u][k] = p.part_lse[sidx];
+            o[u][k] = *reinterpret_cast<const Vec*>(p.part_o + sidx * D + lane * V);
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < kMergeRowBatch; ++u) {
+        float bm = m[u];
+#pragma unroll
+        for (int k = 0; k < kMergePieceBatch; ++k) bm = fmaxf(bm, ls[u][k]);
+        if (bm == -INFINITY) continue;
+        if (bm != m[u]) {
+          const float c = m[u] == -INFINITY ? 0.f : fast_exp2(m[u] - bm);
+          wsum[u] *= c;
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[u][q] *= c;
+          m[u] = bm;
+        }
+#pragma unroll
+        for (int k = 0; k < kMergePieceBatch; ++k) {
+          if (ls[u][k] == -INFINITY) continue;
+          const float w = fast_exp2(ls[u][k] - bm);
+          wsum[u] += w;
+          const float* ov = reinterpret_cast<const float*>(&o[u][k]);
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[u][q] = __fmaf_rn(w, ov[q], acc[u][q]);
+        }
       }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; q += 2) {
-      if (q < per) {
-        const float o0 = acc[q] * inv, o1 = acc[q + 1] * inv;
-        *reinterpret_cast<uint32_t*>(p.out + orow * D + lane * per + q) = pack_bf16x2(o0, o1);
-        if (p.out_sel && i == sel) {
-          float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h) * D + lane * per + q;
+    for (int u = 0; u < kMergeRowBatch; ++u) {
+      if (!live[u]) continue;
+      const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h[u]) * p.C + i[u];
+      const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
+#pragma unroll
+      for (int q = 0; q < V; q += 2) {
+        const float o0 = acc[u][q] * inv, o1 = acc[u][q + 1] * inv;
+        *reinterpret_cast<uint32_t*>(p.out + orow * D + lane * V + q) = pack_bf16x2(o0, o1);
+        if (p.out_sel && i[u] == sel) {
+          float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h[u]) * D + lane * V + q;
           sd[0] = o0;
           sd[1] = o1;
         }
@@ -767,12 +851,13 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long items = (static_cast<long long>(p.B) * (p.Hq + p.Hkv) * p.C) * (p.D / 16);
-  const int blocks = static_cast<int>(min(static_cast<long long>(65535) * 4, (items + 255) / 256));
-  rope_prep_kernel<<<blocks, 256, 0, stream>>>(p);
-  plan_units_kernel<<<1, 1024, 0, stream>>>(p);
+  const long long items = static_cast<long long>(p.B) * ((p.Hq + p.Hkv + kPrepHeads - 1) / kPrepHeads) * p.C *
+                          (p.D / 16);
+  const int rope_blocks =
+      static_cast<int>(max(1LL, min(static_cast<long long>(65535) * 4, (items + kPrepThreads - 1) / kPrepThreads)));
+  prep_kernel<<<rope_blocks + 1, kPrepThreads, 0, stream>>>(p);
   kern<<<p.ctas, kThreadsPair, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  merge_units_kernel<<<dim3(p.units, kUnitRows / 32), 1024, 0, stream>>>(p);
+  merge_units_kernel<D><<<dim3(p.units, kUnitRows / kMergeRows), kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -313,19 +313,31 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // ------------------------------------------------------------------ RoPE
 
+// The 32 table values one 8-element chunk pair needs: cos and sin at dims
+// d..d+7 and at d+D/2..d+D/2+7.
+struct RopeTab {
+  float4 cl0, cl1, sl0, sl1, ch0, ch1, sh0, sh1;
+};
+
+__device__ __forceinline__ RopeTab rope_tab(const float* cos_lo, const float* sin_lo, const float* cos_hi,
+                                            const float* sin_hi) {
+  RopeTab t;
+  t.cl0 = __ldg(reinterpret_cast<const float4*>(cos_lo));
+  t.cl1 = __ldg(reinterpret_cast<const float4*>(cos_lo + 4));
+  t.sl0 = __ldg(reinterpret_cast<const float4*>(sin_lo));
+  t.sl1 = __ldg(reinterpret_cast<const float4*>(sin_lo + 4));
+  t.ch0 = __ldg(reinterpret_cast<const float4*>(cos_hi));
+  t.ch1 = __ldg(reinterpret_cast<const float4*>(cos_hi + 4));
+  t.sh0 = __ldg(reinterpret_cast<const float4*>(sin_hi));
+  t.sh1 = __ldg(reinterpret_cast<const float4*>(sin_hi + 4));
+  return t;
+}
+
 // Rotate one pair of 8-element bf16 chunks (dims d..d+7 and d+D/2..d+D/2+7)
 // with fp32 products and sums, no fused multiply-add, round to nearest even.
-__device__ __forceinline__ void rope_pair(uint4& lo, uint4& hi, const float* cos_lo,
-                                          const float* sin_lo, const float* cos_hi,
-                                          const float* sin_hi) {
-  const float4 cl0 = *reinterpret_cast<const float4*>(cos_lo);
-  const float4 cl1 = *reinterpret_cast<const float4*>(cos_lo + 4);
-  const float4 sl0 = *reinterpret_cast<const float4*>(sin_lo);
-  const float4 sl1 = *reinterpret_cast<const float4*>(sin_lo + 4);
-  const float4 ch0 = *reinterpret_cast<const float4*>(cos_hi);
-  const float4 ch1 = *reinterpret_cast<const float4*>(cos_hi + 4);
-  const float4 sh0 = *reinterpret_cast<const float4*>(sin_hi);
-  const float4 sh1 = *reinterpret_cast<const float4*>(sin_hi + 4);
+__device__ __forceinline__ void rope_apply(uint4& lo, uint4& hi, const RopeTab& t) {
+  const float4 cl0 = t.cl0, cl1 = t.cl1, sl0 = t.sl0, sl1 = t.sl1;
+  const float4 ch0 = t.ch0, ch1 = t.ch1, sh0 = t.sh0, sh1 = t.sh1;
   const float cl[8] = {cl0.x, cl0.y, cl0.z, cl0.w, cl1.x, cl1.y, cl1.z, cl1.w};
   const float sl[8] = {sl0.x, sl0.y, sl0.z, sl0.w, sl1.x, sl1.y, sl1.z, sl1.w};
   const float chh[8] = {ch0.x, ch0.y, ch0.z, ch0.w, ch1.x, ch1.y, ch1.z, ch1.w};
@@ -347,6 +359,11 @@ __device__ __forceinline__ void rope_pair(uint4& lo, uint4& hi, const float* cos
   }
   lo = make_uint4(ya[0], ya[1], ya[2], ya[3]);
   hi = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+__device__ __forceinline__ void rope_pair(uint4& lo, uint4& hi, const float* cos_lo, const float* sin_lo,
+                                          const float* cos_hi, const float* sin_hi) {
+  rope_apply(lo, hi, rope_tab(cos_lo, sin_lo, cos_hi, sin_hi));
 }
 
 }  // namespace cpa
