@@ -47,12 +47,11 @@ KERNEL_SOURCES = {
     "decode": ["decode.cu", "tiles.cuh", "common.cuh", "kernels.h"],
 }
 MEASURED_TRAFFIC = {
-    # long-context chunk call: rope_prep + plan + attn_pair + merge (profiles/dram_traffic_calls.md)
-    "prefill": {"src": "46b30b7784a8c7e9", "bytes": 657603840},
-    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0085 x)
-    "decode": {"src": "ed4fceee0fa400aa", "bytes": 4836855406},
+    # long-context chunk call: prep + attn_pair + merge, one ncu capture of the second call
+    "prefill": {"src": "2f9cb6bc36a8d83e", "bytes": 657344768},
+    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0084 x)
+    "decode": {"src": "7b429be1ffa154a5", "bytes": 4836439267},
 }
-
 
 def source_hash(kind):
     import hashlib
@@ -365,9 +364,115 @@ def ours(args, rank, world, dev):
         "gpu_launches": launches * K,
         "clocks": clk,
     }
+    if not args.no_tail_policy:
+        line["tail_policy"] = measure_tail_policy(cpa, dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(parts, tokens, budget_s=args.cpu_seconds)
     return line
+
+
+# ------------------------------------------------------------------ tail policy
+
+TAIL_TAILS = (1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 127)
+
+
+def _graph_us(fn, reps=20):
+    """Median device time of one replay of `fn` captured in a CUDA graph."""
+    fn()                                   # eager warm-up (kernel attributes, maps)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
+
+
+def measure_tail_policy(cpa, dev, tails=TAIL_TAILS):
+    """Padded versus scalar cost of a prompt's last t tokens on a full
+    sliding-window cache (B=1, 8 q / 1 kv heads, D=256, W=512): padded is
+    snapshot + one chunk attention padded to c_pad rows + padded append +
+    rollback; scalar is t x (decode attention + one-row append).  Each
+    sequence is one CUDA graph, so launch cost is the device's alone."""
+    from synth import normal_bf16, rope_tables
+    B, Hq, Hkv, D, W, C = 1, 8, 1, 256, 512, 128
+    pos0 = 896
+    q = normal_bf16((B, Hq, C, D), 0, "tail_policy/q").to(dev)
+    k = normal_bf16((B, Hkv, C, D), 0, "tail_policy/k").to(dev)
+    v = normal_bf16((B, Hkv, C, D), 0, "tail_policy/v").to(dev)
+    cos, sin = (t.to(dev) for t in rope_tables(np.arange(pos0, pos0 + C)[None, :], D, 10000.0))
+    ck = normal_bf16((B, Hkv, W, D), 0, "tail_policy/ck").to(dev)
+    cv = normal_bf16((B, Hkv, W, D), 0, "tail_policy/cv").to(dev)
+    cache = cpa.KVCache(ck, cv, torch.full((B,), W, dtype=torch.int32, device=dev), cpa.SLIDING, W, 0)
+    err = cpa.new_error_word(dev)
+    scratch = torch.empty(cpa.cache_scratch_size(cache, C), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(1, cpa.attn_workspace_size(B, Hq, Hkv, D, C, W)), dtype=torch.uint8, device=dev)
+    steps = [(q[:, :, i:i + 1].contiguous(), k[:, :, i:i + 1].contiguous(), v[:, :, i:i + 1].contiguous(),
+              cos[:, i:i + 1].contiguous(), sin[:, i:i + 1].contiguous()) for i in range(C)]
+    one = torch.ones((B,), dtype=torch.int32, device=dev)
+    out1 = torch.empty((B, Hq, 1, D), dtype=torch.bfloat16, device=dev)
+
+    def padded_inputs(t, cp):
+        def pad(x):
+            y = torch.zeros(x.shape[:2] + (cp,) + x.shape[3:], dtype=x.dtype, device=dev)
+            y[:, :, :t] = x[:, :, :t]
+            return y
+        return (pad(q), pad(k), pad(v), cos[:, :cp].contiguous(), sin[:, :cp].contiguous(),
+                torch.full((B,), t, dtype=torch.int32, device=dev), torch.full((B,), cp, dtype=torch.int32, device=dev),
+                torch.empty((B, Hq, cp, D), dtype=torch.bfloat16, device=dev))
+
+    def padded_fn(t, cp):
+        qp, kp, vp, cs, sn, nr, full, out = padded_inputs(t, cp)
+
+        def fn():
+            cpa.kv_snapshot_padded_append(cache, nr, cp, scratch, err=err)
+            cpa.chunk_prefill_attn(qp, kp, vp, cs, sn, cache, W, past_len=cache.len, n_real=nr, window=W,
+                                   out=out, workspace=ws, err=err)
+            cpa.kv_append(cache, kp, vp, cs, sn, full, scratch=scratch, err=err)
+            cpa.kv_rollback_padded_append(cache, cp, scratch, err=err)
+        return fn
+
+    def scalar_fn(t):
+        def fn():
+            for i in range(t):
+                qs, ks, vs, cs, sn = steps[i]
+                cpa.decode_step(qs, ks, vs, cs, sn, cache, W, past_len=cache.len, n_real=one, window=W,
+                                out=out1, workspace=ws, err=err)
+                cpa.kv_append(cache, ks, vs, cs, sn, one, scratch=scratch, err=err)
+        return fn
+
+    def bucket(t):
+        cp = 16
+        while cp < t:
+            cp *= 2
+        return min(cp, C)
+
+    rows = []
+    for t in tails:
+        rows.append({"t": t, "scalar_us": round(_graph_us(scalar_fn(t)), 2),
+                     "padded_c128_us": round(_graph_us(padded_fn(t, C)), 2),
+                     "c_pad": bucket(t), "padded_bucket_us": round(_graph_us(padded_fn(t, bucket(t))), 2)})
+    torch.cuda.synchronize()
+    if int(err[0]) != 0:
+        raise RuntimeError(f"tail policy: device error bits {int(err[0])}")
+
+    def crossover(key):
+        for r in rows:
+            if r[key] <= r["scalar_us"]:
+                return r["t"]
+        return None
+    return {"workload": "full sliding cache B1, 8/1 heads, D256, W512; tail of t real tokens",
+            "timing": "one CUDA graph per sequence, median of 20 replays, L2-resident",
+            "crossover_c128": crossover("padded_c128_us"), "crossover_bucket": crossover("padded_bucket_us"),
+            "rows": rows}
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -498,6 +603,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tail-policy", action="store_true", help="skip the padded-vs-scalar tail measurement")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--case", default=None, help="run only this workload's attention call (profiling)")
     ap.add_argument("--reps", type=int, default=2)

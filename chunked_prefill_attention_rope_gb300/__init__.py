@@ -11,6 +11,7 @@ stream.  The entry points mirror include/cpa.h:
     kv_snapshot_padded_append / kv_rollback_padded_append
                          make a padded append to a sliding-window cache
                          byte-identical to an unpadded one
+    tail_plan            padded chunk or one-token steps for a prompt tail
 """
 from __future__ import annotations
 
@@ -25,10 +26,13 @@ __all__ = [
     "decode_step",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
     "attn_workspace_size", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
+    "tail_plan", "TAIL_SCALAR", "TAIL_PADDED", "TAIL_AUTO", "TAIL_FORCE_SCALAR", "TAIL_FORCE_PADDED",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 GLOBAL, SLIDING = 0, 1
+TAIL_SCALAR, TAIL_PADDED = 0, 1
+TAIL_AUTO, TAIL_FORCE_SCALAR, TAIL_FORCE_PADDED = 0, 1, 2
 EBIT = dict(CAPACITY=1, PAST_GT_SPAN=2, NREAL_GT_C=4, SLIDING_N=8, SNAPSHOT=16, TIMEOUT=32)
 
 
@@ -86,11 +90,12 @@ def load_library():
     lib.cpa_cache_scratch_size.restype = sz
     lib.cpa_kv_snapshot_padded_append.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, vp, sz, vp, vp]
     lib.cpa_kv_rollback_padded_append.argtypes = [ctypes.POINTER(_Cache), i32, i32, i32, i32, vp, sz, vp, vp]
+    lib.cpa_tail_plan.argtypes = [i32, i32, i32, i32, vp, i32, i32, i32, vp, vp]
     lib.cpa_status_str.argtypes = [i32]
     lib.cpa_status_str.restype = ctypes.c_char_p
     lib.cpa_version.restype = ctypes.c_char_p
     for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_chunk_prefill_attn_noalloc", "cpa_kv_append",
-              "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append"):
+              "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append", "cpa_tail_plan"):
         getattr(lib, f).restype = i32
     _LIB = lib
     return lib
@@ -256,3 +261,18 @@ def kv_rollback_padded_append(cache: KVCache, C: int, scratch, err=None, stream=
                                              scratch.data_ptr(), scratch.numel(), err.data_ptr(),
                                              _stream(stream)))
     return err
+
+
+def tail_plan(t: int, C: int, window: int = 0, sink: int = 0, buckets=None, crossover: int = 0,
+              force: int = TAIL_AUTO):
+    """(mode, c_pad) for a prompt tail of t real tokens: TAIL_SCALAR with c_pad = t,
+    or TAIL_PADDED with the chunk rows to pad to (cpa_tail_plan)."""
+    lib = load_library()
+    arr = None
+    n = 0
+    if buckets:
+        n = len(buckets)
+        arr = (ctypes.c_int32 * n)(*buckets)
+    mode, c_pad = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.cpa_tail_plan(t, C, window, sink, arr, n, crossover, force, ctypes.byref(mode), ctypes.byref(c_pad)))
+    return mode.value, c_pad.value

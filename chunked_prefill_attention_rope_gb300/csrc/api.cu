@@ -311,6 +311,33 @@ cpa_status cpa_kv_rollback_padded_append(const cpa_cache* cache, int B, int Hkv,
              : CPA_ERR_CUDA;
 }
 
+cpa_status cpa_tail_plan(int t, int C, int window, int sink, const int32_t* buckets, int n_buckets,
+                         int crossover, int force, int32_t* mode, int32_t* c_pad) {
+  if (!mode || !c_pad) return CPA_ERR_NULL;
+  if (C < 1 || t < 1 || t > C || window < 0 || sink < 0 || n_buckets < 0) return CPA_ERR_SHAPE;
+  if (n_buckets > 0 && !buckets) return CPA_ERR_NULL;
+  if (force < CPA_TAIL_AUTO || force > CPA_TAIL_FORCE_PADDED) return CPA_ERR_SHAPE;
+  for (int i = 0; i < n_buckets; ++i) {
+    if (buckets[i] < 1 || buckets[i] > C) return CPA_ERR_SHAPE;
+    if (i > 0 && buckets[i] <= buckets[i - 1]) return CPA_ERR_SHAPE;
+  }
+  *mode = CPA_TAIL_SCALAR;
+  *c_pad = t;
+  if (force == CPA_TAIL_FORCE_SCALAR) return CPA_OK;
+  if (force == CPA_TAIL_AUTO && t < (crossover > 0 ? crossover : CPA_TAIL_CROSSOVER_DEFAULT)) return CPA_OK;
+  // smallest runnable bucket holding the tail whose padded append the window can snapshot
+  const int n = n_buckets > 0 ? n_buckets : 1;
+  for (int i = 0; i < n; ++i) {
+    const int cp = n_buckets > 0 ? buckets[i] : C;
+    if (cp < t) continue;
+    if (window > 0 && window <= cp + sink) continue;
+    *mode = CPA_TAIL_PADDED;
+    *c_pad = cp;
+    return CPA_OK;
+  }
+  return force == CPA_TAIL_FORCE_PADDED ? CPA_ERR_WINDOW_TOO_SMALL : CPA_OK;
+}
+
 const char* cpa_status_str(cpa_status s) {
   switch (s) {
     case CPA_OK: return "ok";

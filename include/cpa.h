@@ -238,6 +238,45 @@ cpa_status cpa_kv_rollback_padded_append(const cpa_cache* cache, int B, int Hkv,
                                          void* scratch, size_t scratch_bytes,
                                          int32_t* err, cpa_stream stream);
 
+/*
+ * Tail policy ([P4, Fix] and the review's padded-versus-scalar sweep; its
+ * follow-up list proposes a small tail-chunk variant).  A runtime whose chunk
+ * calls have fixed shapes feeds the last t real tokens of a prompt either as
+ *   CPA_TAIL_SCALAR: t one-token steps (cpa_decode_step + cpa_kv_append of one
+ *                    row each), or
+ *   CPA_TAIL_PADDED: one chunk of c_pad rows, the t real rows first and zero
+ *                    pad rows after; on a SLIDING cache wrapped in snapshot ->
+ *                    attention -> cpa_kv_append(n_rows = c_pad) -> rollback, on
+ *                    a GLOBAL cache followed by cpa_kv_append(n_rows = t).
+ * Both leave the same cache bytes.  Arguments:
+ *   t          real tail tokens, 1 <= t <= C;
+ *   C          the full chunk rows (c_pad never exceeds it);
+ *   window     W of a SLIDING cache, 0 for a GLOBAL cache;  sink: S (0 if none);
+ *   buckets    the chunk sizes the caller can run, ascending, each in [1, C];
+ *              NULL (n_buckets = 0) means {C} alone;
+ *   crossover  the smallest t for which the padded chunk is faster;
+ *              <= 0 means CPA_TAIL_CROSSOVER_DEFAULT;
+ *   force      CPA_TAIL_AUTO, CPA_TAIL_FORCE_SCALAR (the kill switch) or
+ *              CPA_TAIL_FORCE_PADDED.
+ * Results: *mode and *c_pad (the smallest bucket >= t that a SLIDING cache
+ * can snapshot, i.e. with W > c_pad + S; t for CPA_TAIL_SCALAR).  With no such
+ * bucket the tail runs scalar (AUTO) or the call returns
+ * CPA_ERR_WINDOW_TOO_SMALL (FORCE_PADDED), following [P4, review]'s
+ * sink-aware guard.  Host only: no device memory, no stream.
+ * Returns CPA_ERR_NULL for NULL mode / c_pad, CPA_ERR_SHAPE for t outside
+ * [1, C], an unsorted or out-of-range bucket list, or W < 0, S < 0.
+ */
+#define CPA_TAIL_SCALAR 0
+#define CPA_TAIL_PADDED 1
+#define CPA_TAIL_AUTO 0
+#define CPA_TAIL_FORCE_SCALAR 1
+#define CPA_TAIL_FORCE_PADDED 2
+/* Measured on GB300: D = 256, 8 q / 1 kv heads, a full 512-row window cache,
+ * buckets {16, 32, 64, 128}, every sequence replayed as one CUDA graph. */
+#define CPA_TAIL_CROSSOVER_DEFAULT 2
+cpa_status cpa_tail_plan(int t, int C, int window, int sink, const int32_t* buckets, int n_buckets,
+                         int crossover, int force, int32_t* mode, int32_t* c_pad);
+
 /* Text for a status code (static storage). */
 const char* cpa_status_str(cpa_status status);
 

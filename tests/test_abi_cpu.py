@@ -26,7 +26,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     _, so = lib
     names = declared_functions()
-    assert len(names) == 10, names
+    assert len(names) == 11, names
     for name in names:
         assert hasattr(so, name), name
 
@@ -95,3 +95,44 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(cpa, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         cpa.load_library()
+
+
+def test_tail_plan_policy(lib):
+    """cpa_tail_plan: scalar below the crossover, padded to the smallest
+    bucket at or above it, the sink-aware window guard ("Pad the
+    chunked-prefill tail for sliding-window models", Fix and review), and the
+    kill switch."""
+    cpa, _ = lib
+    S, P = cpa.TAIL_SCALAR, cpa.TAIL_PADDED
+    B4 = [16, 32, 64, 128]
+    # the pages' M4 Pro policy: tails <= 8 stay scalar, padding from 9 up, one 128-row bucket
+    assert cpa.tail_plan(8, 128, 512, 0, crossover=9) == (S, 8)
+    assert cpa.tail_plan(9, 128, 512, 0, crossover=9) == (P, 128)
+    assert cpa.tail_plan(127, 128, 512, 0, crossover=9) == (P, 128)
+    # buckets: the smallest one that holds the tail
+    assert cpa.tail_plan(9, 128, 512, 0, B4, crossover=9) == (P, 16)
+    assert cpa.tail_plan(16, 128, 512, 0, B4, crossover=9) == (P, 16)
+    assert cpa.tail_plan(17, 128, 512, 0, B4, crossover=9) == (P, 32)
+    assert cpa.tail_plan(100, 128, 512, 0, B4, crossover=9) == (P, 128)
+    # library default crossover
+    assert cpa.tail_plan(1, 128, 512, 0, B4) == (S, 1)
+    assert cpa.tail_plan(2, 128, 512, 0, B4) == (P, 16)
+    # sink-aware guard: W <= c_pad + S is never snapshotted; a larger bucket
+    # cannot help, so the tail stays scalar (or a forced pad is refused)
+    assert cpa.tail_plan(20, 32, 40, 0, [16, 32], crossover=9) == (P, 32)
+    assert cpa.tail_plan(20, 32, 40, 8, [16, 32], crossover=9) == (S, 20)
+    assert cpa.tail_plan(12, 32, 40, 8, [16, 32], crossover=9) == (P, 16)
+    with pytest.raises(cpa.CpaError) as e:
+        cpa.tail_plan(20, 32, 40, 8, [16, 32], force=cpa.TAIL_FORCE_PADDED)
+    assert e.value.status == 5
+    # global caches have no window guard
+    assert cpa.tail_plan(20, 32, 0, 0, [16, 32], crossover=9) == (P, 32)
+    # kill switch and forced padding
+    assert cpa.tail_plan(127, 128, 512, 0, B4, force=cpa.TAIL_FORCE_SCALAR) == (S, 127)
+    assert cpa.tail_plan(1, 128, 512, 0, B4, force=cpa.TAIL_FORCE_PADDED) == (P, 16)
+    # bad arguments
+    for bad in (dict(t=0, C=128), dict(t=129, C=128), dict(t=4, C=128, buckets=[32, 16]),
+                dict(t=4, C=128, buckets=[16, 256]), dict(t=4, C=128, window=-1), dict(t=4, C=128, force=3)):
+        with pytest.raises(cpa.CpaError) as e:
+            cpa.tail_plan(**bad)
+        assert e.value.status == 2, bad

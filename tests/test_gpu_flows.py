@@ -93,9 +93,11 @@ def test_invariant_a_full_chunked_decode_on_gpu():
         assert_close(out, ref, f"flow_a/{name}")
 
 
-def run_sliding_flow(cpa, prefix, tail, padded_tail=True, Hq=8, D=256, W=512, C=128):
+def run_sliding_flow(cpa, prefix, tail, padded_tail=True, Hq=8, D=256, W=512, C=128, c_tail=None):
     """GPU and oracle side by side: `prefix` full chunks, then a tail of `tail`
-    tokens (padded chunk with snapshot/rollback, or scalar decode steps)."""
+    tokens (a chunk padded to `c_tail` rows, default C, with snapshot/rollback,
+    or scalar decode steps)."""
+    c_tail = c_tail or C
     Hkv = 1
     N = prefix * C + tail
     q = normal_bf16((1, Hq, N, D), 0, "flow_b/q")
@@ -134,11 +136,11 @@ def run_sliding_flow(cpa, prefix, tail, padded_tail=True, Hq=8, D=256, W=512, C=
     if tail:
         if padded_tail:
             nr = torch.tensor([tail], dtype=torch.int32, device=DEV)
-            full = torch.tensor([C], dtype=torch.int32, device=DEV)
-            err = cpa.kv_snapshot_padded_append(cache, nr, C, scratch)
-            _, kc, vc, cs, sn, _ = attend(s, tail, C)
+            full = torch.tensor([c_tail], dtype=torch.int32, device=DEV)
+            err = cpa.kv_snapshot_padded_append(cache, nr, c_tail, scratch)
+            _, kc, vc, cs, sn, _ = attend(s, tail, c_tail)
             cpa.kv_append(cache, d(kc), d(vc), d(cs), d(sn), full, scratch=scratch, err=err)
-            cpa.kv_rollback_padded_append(cache, C, scratch, err=err)
+            cpa.kv_rollback_padded_append(cache, c_tail, scratch, err=err)
             torch.cuda.synchronize()
             assert int(err[0]) == 0
             O.kv_append_sliding(ok_, ov_, ol, bf16_bits(kc), bf16_bits(vc), cs.numpy(), sn.numpy(), [tail], W)
@@ -167,3 +169,17 @@ def test_sliding_1023_token_prompt_padded_tail_equals_scalar_tail():
 def test_sliding_tail_sweep(prefix, tail):
     cpa = lib()
     run_sliding_flow(cpa, prefix, tail, padded_tail=True, Hq=4, D=128)
+
+
+@pytest.mark.parametrize("tail", [2, 9, 20, 33, 100])
+def test_sliding_tail_padded_to_plan_bucket(tail):
+    """The tail chunk size cpa_tail_plan picks from buckets {16, 32, 64, 128}
+    ("Pad the chunked-prefill tail for sliding-window models", follow-ups: a
+    small tail-chunk variant): the padded tail in that bucket leaves the same
+    cache bytes as the oracle's exact append and as the scalar tail."""
+    cpa = lib()
+    mode, c_pad = cpa.tail_plan(tail, 128, 512, 0, [16, 32, 64, 128], crossover=2)
+    assert mode == cpa.TAIL_PADDED and c_pad >= tail and c_pad == max(16, 1 << (tail - 1).bit_length())
+    kp, vp = run_sliding_flow(cpa, 7, tail, padded_tail=True, c_tail=c_pad)
+    ks, vs = run_sliding_flow(cpa, 7, tail, padded_tail=False)
+    assert np.array_equal(kp, ks) and np.array_equal(vp, vs)
