@@ -155,6 +155,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank sets the job's time)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 class Part:
     pass
 
@@ -316,10 +325,7 @@ def ours(args, rank, world, dev):
     torch.cuda.synchronize()
     if int(err[0]) != 0:
         raise RuntimeError(f"device error bits {int(err[0])}")
-    times = torch.tensor([ms, ms_e2e, t_pf, t_dc], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms, ms_e2e, t_pf, t_dc = times.tolist()
+    ms, ms_e2e, t_pf, t_dc = max_over_ranks([ms, ms_e2e, t_pf, t_dc], world, dev)
     if rank != 0:
         return None
     hbm, tf_burst, tf_sus, src = load_peaks()
@@ -366,6 +372,7 @@ def ours(args, rank, world, dev):
     }
     if not args.no_tail_policy:
         line["tail_policy"] = measure_tail_policy(cpa, dev)
+        line["page1"] = measure_page1(cpa, dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(parts, tokens, budget_s=args.cpu_seconds)
     return line
@@ -473,6 +480,78 @@ def measure_tail_policy(cpa, dev, tails=TAIL_TAILS):
             "timing": "one CUDA graph per sequence, median of 20 replays, L2-resident",
             "crossover_c128": crossover("padded_c128_us"), "crossover_bucket": crossover("padded_bucket_us"),
             "rows": rows}
+
+
+# ------------------------------------------------------------------ page-1 call shape
+
+def additive_mask(L, n, C, P, Hq, W):
+    """[1, Hq, C, P+C] fp32 additive mask of one sequence: 0 where the key is
+    visible (past slot j < L within the window, chunk row t < n with t <= i
+    within the window), -1e30 elsewhere."""
+    i = torch.arange(C)[:, None]
+    j = torch.arange(P + C)[None, :]
+    t = j - P
+    in_win = lambda d: torch.ones_like(d, dtype=torch.bool) if W == 0 else d < W
+    vis = torch.where(j < P, (j < L) & in_win(L + i - j), (t < n) & (t <= i) & in_win(i - t))
+    m = torch.where(vis, torch.tensor(0.0), torch.tensor(-1e30)).to(torch.float32)
+    return m[None, None].expand(1, Hq, C, P + C).contiguous()
+
+
+def measure_page1(cpa, dev, reps=10):
+    """The page-1 call shape: 18 layers, each an attention call with an
+    explicit mask and a selected row plus a global append (D=256, 4/1 heads,
+    800 cached rows, 52 real rows padded to 64, layers alternating a 512-row
+    window with base 1e4 and global attention with base 1e6).  Timed eager and
+    as one CUDA graph replay; median of `reps`."""
+    from synth import rope_tables
+    w = WORKLOADS["page1"]
+    L, n = int(w.past_lens()[0]), int(w.n_reals()[0])
+    shared = {}
+    for kind, W, base in (("sliding", 512, 1e4), ("global", 0, 1e6)):
+        cos, sin = rope_tables(np.arange(L, L + w.C)[None, :], w.D, base)
+        shared[kind] = (additive_mask(L, n, w.C, w.P, w.Hq, W).to(dev), cos.to(dev), sin.to(dev))
+    len0 = torch.full((1,), L, dtype=torch.int32, device=dev)
+    n_real = torch.full((1,), n, dtype=torch.int32, device=dev)
+    sel_row = torch.full((1,), n - 1, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(1, cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)), dtype=torch.uint8,
+                     device=dev)
+    err = cpa.new_error_word(dev)
+    layers = []
+    for layer in range(w.layers):
+        inp = make_chunk_inputs(w, layer=layer, device=dev)
+        ck, cv = make_cache(w, layer=layer, device=dev)
+        layers.append(("sliding" if layer % 2 == 0 else "global", inp, cpa.KVCache(ck, cv, len0.clone()),
+                       torch.empty((1, w.Hq, w.C, w.D), dtype=torch.bfloat16, device=dev),
+                       torch.empty((1, w.Hq * w.D), dtype=torch.float32, device=dev)))
+
+    def run():
+        for kind, inp, cache, out, sel in layers:
+            mask, cos, sin = shared[kind]
+            cache.len.copy_(len0)
+            cpa.chunk_prefill_attn(inp["q"], inp["k"], inp["v"], cos, sin, cache, w.P, past_len=len0,
+                                   n_real=n_real, mask=mask, sel_row=sel_row, out=out, out_sel=sel,
+                                   workspace=ws, err=err)
+            cpa.kv_append(cache, inp["k"], inp["v"], cos, sin, n_real, err=err)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    eager = statistics.median(ts)
+    graph = _graph_us(run, reps)
+    if int(err[0]) != 0:
+        raise RuntimeError(f"page-1 shape: device error bits {int(err[0])}")
+    return {"workload": "page-1 call shape: 18 layers x (attention with explicit mask + select, global append); "
+                        "B1, 4/1 heads, D256, past 800, C64 (52 real)",
+            "eager_us_per_layer": round(eager / w.layers, 2), "graph_us_per_layer": round(graph / w.layers, 2),
+            "timing": "CUDA events, median of 10; graph = the 18 layers captured once and replayed; L2-resident"}
 
 
 # ------------------------------------------------------------------ oracle arm
