@@ -57,6 +57,7 @@ enum Path { kPathSingle = 0, kPathPair = 1, kPathDecode = 2 };
 
 struct Geometry {
   int G, R, nq, splits, path;
+  bool cluster;  // single-tile splits merged inside a thread-block cluster
   PairTeams teams;
 };
 
@@ -74,6 +75,7 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   g.R = 128 / g.G;
   g.nq = (C + g.R - 1) / g.R;
   g.teams = PairTeams{};
+  g.cluster = false;
   const int sms = num_sms();
   if (attn_uses_pair(D, g.nq) && !attn_uses_decode(D, C, g.G)) {
     g.path = kPathPair;
@@ -89,12 +91,14 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   while (ctas * s < 2LL * sms && s * 2 <= max_tiles) s *= 2;
   if (g.nq == 1 && max_tiles > 32) s = max(s, (max_tiles + 15) / 16);
   g.splits = max(1, min(s, max(1, max_tiles)));
+  g.cluster = g.path == kPathSingle && (g.splits == 2 || g.splits == 4 || g.splits == 8) &&
+              attn_cluster_ok(D, g.splits);
   return g;
 }
 
 size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
   if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, D, C, g.teams).total;
-  if (g.splits <= 1) return 0;
+  if (g.splits <= 1 || g.cluster) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * C;
   const size_t o = static_cast<size_t>(g.splits) * rows * D * sizeof(float);
   const size_t lse = static_cast<size_t>(g.splits) * rows * sizeof(float);
@@ -177,6 +181,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   p.R = g.R;
   p.nq = g.nq;
   p.splits = g.splits;
+  p.cluster = g.cluster ? 1 : 0;
   const double scale = a->scale > 0.f ? static_cast<double>(a->scale) : 1.0 / sqrt(static_cast<double>(a->D));
   p.sl2 = static_cast<float>(scale * 1.4426950408889634);
   p.q = static_cast<const uint16_t*>(a->q);
@@ -215,7 +220,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
         !make_map(&pm[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G))
       return CPA_ERR_CUDA;
     return launch_attn_pair5(pm, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
-  } else if (g.splits > 1) {
+  } else if (g.splits > 1 && !g.cluster) {
     const size_t rows = static_cast<size_t>(a->B) * a->Hq * a->C;
     const size_t o = static_cast<size_t>(g.splits) * rows * a->D * sizeof(float);
     p.part_o = static_cast<float*>(a->workspace);

@@ -11,8 +11,15 @@
 // and V tiles are loaded once for the whole GQA group.  Key tiles of BN keys
 // are visited chunk tiles first, then past tiles; tiles that the implicit mask
 // leaves fully masked for every row of the CTA are never visited.  A CTA may
-// take only a slice of its key tiles (split-KV); the slices are merged by
-// combine_kernel.
+// take only a slice of its key tiles (split-KV).  With S = 2, 4 or 8 splits,
+// the splits of a query tile form one thread-block cluster: once every CTA
+// of the cluster is done with its Q/K/V buffers, each thread stores its
+// normalised row and log2-sum-exp straight from tensor memory into the
+// shared memory of the CTA that owns the row's slice (CTA s owns rows
+// [s*128/S, (s+1)*128/S)); after a second cluster barrier each CTA merges its
+// slice from its own shared memory.  Other split counts write the partials
+// to the workspace and combine_kernel merges them.  Both merges take the
+// splits in the same fixed order with the same arithmetic.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: K and V tiles into a 2-stage shared-memory ring.
@@ -23,7 +30,8 @@
 //               chunk-K tile in place, applies the mask, keeps the running
 //               max / sum in fp32 (log2 domain, rescaling O only when the max
 //               grows by more than 2^8), writes P as bf16, and finally scales
-//               O by 1/l and stores it.
+//               O by 1/l into a shared-memory staging tile, from which whole
+//               rows are stored (or merged) with coalesced accesses.
 #include "tiles.cuh"
 
 namespace cpa {
@@ -53,6 +61,23 @@ struct AttnSmem {
   static constexpr int kBars = kP + kPBytes;
   static constexpr int kTotal = kBars + static_cast<int>(sizeof(AttnBars));
   static constexpr int kAlloc = kTotal + 1024;  // room to align the base to 1024
+  // Epilogue buffers over the Q/K/V buffers (free once the last product has
+  // finished).  Without a cluster: a staging tile [128][D + 4] fp32 (a
+  // 16-byte pad per row keeps row-per-thread float4 writes conflict-free) and
+  // the rows' log2-sum-exp.  With a cluster of S: the receive buffer of this
+  // CTA's slice, [S][D/4][128/S] float4 with the slot index XOR-swizzled by
+  // the chunk index, then [S][128/S] log2-sum-exp.
+  static constexpr int kStg = D + 4;
+  static constexpr int kStgLse = kBM * kStg * 4;
+  static_assert(kStgLse + kBM * 4 <= kP, "staging tile fits over Q, K and V");
+  static constexpr int kRecvLse = kBM * D * 4;
+  static_assert(kRecvLse + kBM * 4 <= kP, "receive buffer fits over Q, K and V");
+  // Per-row tables over the P buffer: output row index (-1: no such row),
+  // chunk row, (sequence, head) index.
+  static constexpr int kTabRow = kP;
+  static constexpr int kTabI = kTabRow + kBM * 8;
+  static constexpr int kTabBh = kTabI + kBM * 4;
+  static_assert(kTabBh + kBM * 4 <= kP + kPBytes, "row tables fit over P");
   static constexpr int kSCol = 0;               // S buffers at columns [0, 2*BN)
   static constexpr int kOCol = 2 * BN;          // O at columns [2*BN, 2*BN + D)
   static_assert(2 * BN + D <= 512, "TMEM columns");
@@ -209,45 +234,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = g < p.G && i < p.C;
     const int h = kvh * p.G + (valid ? g : 0);
 
-    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.  The
-    // G heads of chunk row i share its table row: each item loads the tables
-    // of one (row, chunk pair) once and rotates that pair for every head, the
-    // loads of four heads issued together.
+    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.  An
+    // item is one (chunk row, 8-dim chunk pair, group of four heads): the
+    // heads share the row's table values, loaded once per item.  Each thread
+    // keeps two items' loads in flight before rotating either.
     {
       const int R = p.R;
-      for (int item = tid; item < R * (D / 16); item += 128) {
-        const int il = item / (D / 16);
-        const int kc = item % (D / 16);
-        const int kh = kc + D / 16;
-        const int ri = qt * R + il;
-        const bool in = ri < p.C;
-        RopeTab tab{};
-        if (in) {
-          const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-          const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-          tab = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-        }
-        for (int g0 = 0; g0 < p.G; g0 += 4) {
-          uint4 lo[4], hi[4];
+      const int HG = (p.G + 3) / 4;
+      const int n_items = R * (D / 16) * HG;
+      constexpr int kQU = 2;
+      for (int it0 = tid; it0 < n_items; it0 += 128 * kQU) {
+        RopeTab tab[kQU];
+        uint4 lo[kQU][4], hi[kQU][4];
+        int il[kQU], kc[kQU], g0[kQU];
+        bool in[kQU];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            lo[u] = make_uint4(0, 0, 0, 0);
-            hi[u] = lo[u];
-            const int g = g0 + u;
-            if (in && g < p.G) {
-              const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.C + ri) * D;
-              lo[u] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + kc * 8));
-              hi[u] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc * 8));
-            }
+        for (int u = 0; u < kQU; ++u) {
+          const int item = it0 + 128 * u;
+          kc[u] = item % (D / 16);
+          const int t = item / (D / 16);
+          g0[u] = (t % HG) * 4;
+          il[u] = t / HG;
+          const int ri = qt * R + il[u];
+          in[u] = item < n_items && ri < p.C;
+          if (in[u]) {
+            const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
+            const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
+            tab[u] = rope_tab(cr + kc[u] * 8, sr + kc[u] * 8, cr + D / 2 + kc[u] * 8, sr + D / 2 + kc[u] * 8);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int g = g0 + u;
+          for (int v = 0; v < 4; ++v) {
+            lo[u][v] = make_uint4(0, 0, 0, 0);
+            hi[u][v] = lo[u][v];
+            const int g = g0[u] + v;
+            if (in[u] && g < p.G) {
+              const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.C + ri) * D;
+              lo[u][v] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + kc[u] * 8));
+              hi[u][v] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc[u] * 8));
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kQU; ++u) {
+          if (it0 + 128 * u >= n_items) break;
+          const int kh = kc[u] + D / 16;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int g = g0[u] + v;
             if (g >= p.G) break;
-            if (in) rope_apply(lo[u], hi[u], tab);
-            const int r = g * R + il;
-            *reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8)) = lo[u];
-            *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi[u];
+            if (in[u]) rope_apply(lo[u][v], hi[u][v], tab[u]);
+            const int r = g * R + il[u];
+            *reinterpret_cast<uint4*>(sQ + (kc[u] / 8) * (kBM * 128) + sw128(r, kc[u] % 8)) = lo[u][v];
+            *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi[u][v];
           }
         }
       }
@@ -318,6 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         mbar_arrive(&bars->k_rot[st]);
       }
+      // Explicit mask values of this tile, loaded before the wait on S so
+      // their latency hides behind the product (64-key tiles only: a 128-key
+      // tile has no registers to spare).
+      constexpr bool kMaskEarly = BN == 64;
+      float mk[kMaskEarly ? BN : 1];
+      if (kMaskEarly && mrow) {
+        const int lim = chunk ? p.C : p.P;
+        const float* mp = mrow + (chunk ? p.P + base : base);
+#pragma unroll
+        for (int e = 0; e < (kMaskEarly ? BN : 1); ++e) mk[e] = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+      }
       if (!(ok = warp_all(mbar_wait(&bars->s_full[sb], (q >> 1) & 1, abort)))) break;
       tc_fence_after();
       float x[BN];
@@ -339,7 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* mp = mrow + (pastt ? base : p.P + base);
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
-          const float mv = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+          float mv;
+          if constexpr (kMaskEarly) mv = mk[e];
+          else mv = (base + e < lim) ? __ldg(mp + e) : -1e30f;
           x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(mv, kLog2e));
         }
       } else {
@@ -407,49 +458,172 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const bool empty = !(my_nt > 0 && ok && m_run > kEmptyRow);
     const float inv_l = empty ? 0.f : 1.f / l_run;
-    const int sel = valid ? (p.sel_row ? p.sel_row[b] : tp.n - 1) : -1;
-    const size_t orow = ((static_cast<size_t>(b) * p.Hq + h) * p.C + i);
+    // O / l of this row into the staging tile.  Every product has finished
+    // (pv_done of the last tile) and every copy has been consumed, so the
+    // Q, K and V buffers are free.
+    long long* tab_row = reinterpret_cast<long long*>(smem + SM::kTabRow);
+    int* tab_i = reinterpret_cast<int*>(smem + SM::kTabI);
+    int* tab_bh = reinterpret_cast<int*>(smem + SM::kTabBh);
+    const long long orow_me = (static_cast<long long>(b) * p.Hq + h) * p.C + i;
+    const float lse_me = empty ? -INFINITY : m_run + __log2f(l_run);
+    tab_row[row] = valid ? orow_me : -1;
+    tab_i[row] = i;
+    tab_bh[row] = b * p.Hq + h;
+    if (!p.cluster) {
+      float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o32[32];
-      if (my_nt > 0) {
-        tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c, o32);
-        tmem_ld_wait(o32);
-      }
-      float o[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : __uint_as_float(o32[e]) * inv_l;
-      if (!valid) continue;
-      if (p.part_o) {
-        float* dst = p.part_o + ((static_cast<size_t>(split) * p.B * p.Hq * p.C) + orow) * D + 32 * c;
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-      } else {
-        uint16_t* dst = p.out + orow * D + 32 * c;
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w;
-          w.x = pack_bf16x2(o[e + 0], o[e + 1]);
-          w.y = pack_bf16x2(o[e + 2], o[e + 3]);
-          w.z = pack_bf16x2(o[e + 4], o[e + 5]);
-          w.w = pack_bf16x2(o[e + 6], o[e + 7]);
-          *reinterpret_cast<uint4*>(dst + e) = w;
+      for (int c = 0; c < D / 32; c += 2) {
+        uint32_t o0[32], o1[32];
+        if (my_nt > 0) {
+          tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c, o0);
+          tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c + 32, o1);
+          tmem_ld_wait(o0);
+          tmem_ld_wait(o1);
         }
-        if (p.out_sel && i == sel) {
-          float* sd = p.out_sel + (static_cast<size_t>(b) * p.Hq + h) * D + 32 * c;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(sd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        for (int e = 0; e < 64; e += 4) {
+          const uint32_t* oo = e < 32 ? o0 + e : o1 + (e - 32);
+          float4 v;
+          v.x = empty ? 0.f : __uint_as_float(oo[0]) * inv_l;
+          v.y = empty ? 0.f : __uint_as_float(oo[1]) * inv_l;
+          v.z = empty ? 0.f : __uint_as_float(oo[2]) * inv_l;
+          v.w = empty ? 0.f : __uint_as_float(oo[3]) * inv_l;
+          *reinterpret_cast<float4*>(stg + row * SM::kStg + 32 * c + e) = v;
         }
       }
-    }
-    if (valid && p.part_lse) {
-      p.part_lse[static_cast<size_t>(split) * p.B * p.Hq * p.C + orow] =
-          empty ? -INFINITY : m_run + __log2f(l_run);
+      if (valid && p.part_o) p.part_lse[static_cast<size_t>(split) * p.B * p.Hq * p.C + orow_me] = lse_me;
+      named_bar_sync(1, 128);
+      // This warp's own 32 rows, whole rows with lanes across D: bf16 output
+      // (one split) or fp32 partials.  Row indices come from the table, four
+      // rows per step.
+      const int w = warp - 2;
+      const int sel = p.sel_row ? p.sel_row[b] : tp.n - 1;
+      const size_t part_base = static_cast<size_t>(split) * p.B * p.Hq * p.C;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const int r = 32 * w + k;
+        const long long orow = tab_row[r];
+        if (orow < 0) continue;
+        const float* src = stg + r * SM::kStg;
+        if (p.part_o) {
+          float* dst = p.part_o + (part_base + static_cast<size_t>(orow)) * D;
+#pragma unroll
+          for (int e = 4 * lane; e < D; e += 128)
+            *reinterpret_cast<float4*>(dst + e) = *reinterpret_cast<const float4*>(src + e);
+        } else {
+          uint16_t* dst = p.out + static_cast<size_t>(orow) * D;
+#pragma unroll
+          for (int e = 4 * lane; e < D; e += 128) {
+            const float4 v = *reinterpret_cast<const float4*>(src + e);
+            *reinterpret_cast<uint2*>(dst + e) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+          }
+          if (p.out_sel && tab_i[r] == sel) {
+            float* sd = p.out_sel + static_cast<size_t>(tab_bh[r]) * D;
+#pragma unroll
+            for (int e = 4 * lane; e < D; e += 128)
+              *reinterpret_cast<float4*>(sd + e) = *reinterpret_cast<const float4*>(src + e);
+          }
+        }
+      }
+    } else {
+      // Cluster merge, step 1: once every CTA is done with its Q/K/V
+      // buffers (barrier A), push this row to its slice owner.
+      const int S = p.splits;
+      const int rows_per = kBM / S;
+      const int owner = row / rows_per, slot = row % rows_per;
+      named_bar_sync(1, 128);
+      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+      const uint32_t dst = dsmem_addr(smem_u32(smem), owner);
+      dsmem_st(dst + SM::kRecvLse + 4u * (split * rows_per + slot), lse_me);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o32[32];
+        if (my_nt > 0) {
+          tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c, o32);
+          tmem_ld_wait(o32);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int e = 8 * c + q4;  // float4 chunk index along D
+          float4 v;
+          v.x = empty ? 0.f : __uint_as_float(o32[4 * q4 + 0]) * inv_l;
+          v.y = empty ? 0.f : __uint_as_float(o32[4 * q4 + 1]) * inv_l;
+          v.z = empty ? 0.f : __uint_as_float(o32[4 * q4 + 2]) * inv_l;
+          v.w = empty ? 0.f : __uint_as_float(o32[4 * q4 + 3]) * inv_l;
+          const uint32_t off = 16u * ((split * (D / 4) + e) * rows_per + (slot ^ (e & 7)));
+          dsmem_st4(dst + off, v);
+        }
+      }
     }
   }
 
+  __syncwarp();
+  if (p.cluster) {
+    // Warps 0 and 1 take part in barrier A here; the softmax warps have
+    // passed it above.  Barrier B: every row's partials are in its owner.
+    if (warp < 2)
+      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_sync_all();
+    if (warp >= 2) {
+      // Step 2: merge this CTA's slice from its own shared memory, splits in
+      // order; lanes across D (one float4 chunk per lane and step).
+      const int S = p.splits;
+      const int rows_per = kBM / S;
+      const int w = warp - 2;
+      const int sel = p.sel_row ? p.sel_row[b] : tp.n - 1;
+      const long long* tab_row = reinterpret_cast<const long long*>(smem + SM::kTabRow);
+      const int* tab_i = reinterpret_cast<const int*>(smem + SM::kTabI);
+      const int* tab_bh = reinterpret_cast<const int*>(smem + SM::kTabBh);
+      const float* rlse = reinterpret_cast<const float*>(smem + SM::kRecvLse);
+      constexpr int NCH = D / 4;                      // float4 chunks per row
+      constexpr int CPL = NCH >= 32 ? NCH / 32 : 1;   // chunks per lane
+      for (int j = w; j < rows_per; j += 4) {
+        const int r = split * rows_per + j;
+        const long long orow = tab_row[r];
+        if (orow < 0) continue;
+        float ls[kMaxClusterSplits];
+        float lmax = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          ls[s2] = s2 < S ? rlse[s2 * rows_per + j] : -INFINITY;
+          lmax = fmaxf(lmax, ls[s2]);
+        }
+        float4 acc[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        if (lmax != -INFINITY && lane < NCH) {
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+            if (s2 >= S || ls[s2] == -INFINITY) continue;
+            const float wgt = fast_exp2(ls[s2] - lmax);
+            wsum += wgt;
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+              const int e = lane + 32 * q;
+              const float4 v = *reinterpret_cast<const float4*>(
+                  smem + 16u * ((s2 * NCH + e) * rows_per + (j ^ (e & 7))));
+              acc[q].x = __fmaf_rn(wgt, v.x, acc[q].x);
+              acc[q].y = __fmaf_rn(wgt, v.y, acc[q].y);
+              acc[q].z = __fmaf_rn(wgt, v.z, acc[q].z);
+              acc[q].w = __fmaf_rn(wgt, v.w, acc[q].w);
+            }
+          }
+        }
+        if (lane >= NCH) continue;
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const bool is_sel = p.out_sel && tab_i[r] == sel;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+          const int e = lane + 32 * q;
+          const float4 o = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+          *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(orow) * D + 4 * e) =
+              make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+          if (is_sel) *reinterpret_cast<float4*>(p.out_sel + static_cast<size_t>(tab_bh[r]) * D + 4 * e) = o;
+        }
+      }
+    }
+  }
   __syncthreads();
   if (threadIdx.x == 0 && bars->abort) set_err(p.err, CPA_EBIT_TIMEOUT);
   if (warp == 1) {
@@ -520,8 +694,51 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
     attr_set = true;
   }
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
+  if (p.cluster) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SM::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
+  }
   kern<<<grid, kThreads, SM::kAlloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
+}
+
+// Whether clusters of `splits` CTAs of attn_kernel<D, BN> fit on the device.
+template <int D, int BN>
+static bool cluster_fits(int splits) {
+  using SM = AttnSmem<D, BN>;
+  auto kern = attn_kernel<D, BN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SM::kAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n > 0;
 }
 
 static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
@@ -533,6 +750,31 @@ static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
 }
 
 int attn_block_n(int D) { return D == 256 ? 64 : 128; }
+
+bool attn_cluster_ok(int D, int splits) {
+  if (splits < 2 || splits > kMaxClusterSplits) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  // per device, head dim and split count: 0 unknown, 1 fits, 2 does not
+  static signed char known[16][3][kMaxClusterSplits + 1] = {};
+  const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
+  if (dev < 0 || dev >= 16) return false;
+  signed char& k = known[dev][di][splits];
+  if (k == 0) {
+    bool fits = false;
+    switch (D) {
+      case 64: fits = cluster_fits<64, 128>(splits); break;
+      case 128: fits = cluster_fits<128, 128>(splits); break;
+      case 256: fits = cluster_fits<256, 64>(splits); break;
+      default: break;
+    }
+    k = fits ? 1 : 2;
+  }
+  return k == 1;
+}
 
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   cudaError_t e;
@@ -546,7 +788,7 @@ cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream
       default: return cudaErrorInvalidValue;
     }
   }
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess || p.splits == 1 || p.cluster) return e;
   return launch_combine(p, stream);
 }
 

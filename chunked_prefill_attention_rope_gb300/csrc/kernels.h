@@ -36,6 +36,8 @@ struct AttnParams {
   uint16_t* q_rot;        // rotated queries [B, Hq, C, D] (workspace)
   uint16_t* k_rot;        // rotated chunk keys [B, Hkv, C, D] (workspace)
   int32_t* ptag;          // [2 * ctas] unit of each CTA's partial slots (-1: none)
+  int cluster;            // single-tile path: the splits of a query tile form one
+                          // thread-block cluster and merge their partials in-kernel
 };
 
 // Team-aligned stream-K layout for these sizes, and its workspace.
@@ -52,6 +54,12 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 
 int attn_block_n(int D);
+// Largest split count whose partials the single-tile kernel merges inside a
+// thread-block cluster (portable cluster size).
+constexpr int kMaxClusterSplits = 8;
+// True when clusters of `splits` single-tile CTAs of head dim D can run on the
+// current device (checked once per device and size).
+bool attn_cluster_ok(int D, int splits);
 // True when the two-query-tile kernel (256 packed rows per CTA) serves these sizes.
 inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >= 2; }
 // True when the warp-MMA decode kernel (64-key tiles, G <= 16 rows) serves these sizes.
