@@ -96,13 +96,33 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   return g;
 }
 
+// Workspace of the decode and single-tile paths: split-KV partials (when
+// combine_kernel merges them), then the rotated chunk keys (single-tile path).
+struct SingleWorkspace {
+  size_t part_o, part_lse, k_rot, total;
+};
+SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  SingleWorkspace w{};
+  size_t off = 0;
+  if (g.splits > 1 && !g.cluster) {
+    const size_t rows = static_cast<size_t>(B) * Hq * C;
+    w.part_o = off;
+    off += al(static_cast<size_t>(g.splits) * rows * D * sizeof(float));
+    w.part_lse = off;
+    off += al(static_cast<size_t>(g.splits) * rows * sizeof(float));
+  }
+  if (g.path == kPathSingle) {
+    w.k_rot = off;
+    off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
+  }
+  w.total = off;
+  return w;
+}
+
 size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
   if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, D, C, g.teams).total;
-  if (g.splits <= 1 || g.cluster) return 0;
-  const size_t rows = static_cast<size_t>(B) * Hq * C;
-  const size_t o = static_cast<size_t>(g.splits) * rows * D * sizeof(float);
-  const size_t lse = static_cast<size_t>(g.splits) * rows * sizeof(float);
-  return ((o + 255) & ~size_t(255)) + lse;
+  return single_workspace(g, B, Hq, Hkv, D, C).total;
 }
 
 bool valid_d(int D) { return D == 64 || D == 128 || D == 256; }
@@ -220,11 +240,19 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
         !make_map(&pm[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G))
       return CPA_ERR_CUDA;
     return launch_attn_pair5(pm, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
-  } else if (g.splits > 1 && !g.cluster) {
-    const size_t rows = static_cast<size_t>(a->B) * a->Hq * a->C;
-    const size_t o = static_cast<size_t>(g.splits) * rows * a->D * sizeof(float);
-    p.part_o = static_cast<float*>(a->workspace);
-    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + ((o + 255) & ~size_t(255)));
+  }
+  const SingleWorkspace L = single_workspace(g, a->B, a->Hq, a->Hkv, a->D, a->C);
+  uint8_t* w = static_cast<uint8_t*>(a->workspace);
+  if (g.splits > 1 && !g.cluster) {
+    p.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+  }
+  if (g.path == kPathSingle) {
+    // raw Q rows (box {64, R, G, 1}); chunk keys from the rotated copy
+    p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
+    if (!make_map(&maps[4], a->q, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G) ||
+        !make_map(&maps[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn))
+      return CPA_ERR_CUDA;
   }
   return launch_attn(maps, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }

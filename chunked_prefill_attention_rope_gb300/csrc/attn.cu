@@ -21,13 +21,19 @@
 // to the workspace and combine_kernel merges them.  Both merges take the
 // splits in the same fixed order with the same arithmetic.
 //
+// Chunk keys: rope_chunk_k_kernel rotates them once per call into the
+// workspace (the append's arithmetic).  The attention grid is launched as a
+// programmatic dependent of it, so its prologue and Q rotation run while the
+// keys are rotated; the producer waits for that grid only before its first
+// chunk-key copy.
+//
 // Warp roles (192 threads):
 //   warp 0      TMA producer: K and V tiles into a 2-stage shared-memory ring.
 //   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM S buffers,
 //               O += P V into the TMEM O accumulator; owns the TMEM allocation.
 //   warps 2..5  softmax warpgroup: thread = TMEM lane = packed query row.
-//               Rotates Q into shared memory at the start, rotates each raw
-//               chunk-K tile in place, applies the mask, keeps the running
+//               Rotates the TMA-loaded Q rows in shared memory at the start,
+//               applies the mask, keeps the running
 //               max / sum in fp32 (log2 domain, rescaling O only when the max
 //               grows by more than 2^8), writes P as bf16, and finally scales
 //               O by 1/l into a shared-memory staging tile, from which whole
@@ -41,9 +47,9 @@ constexpr int kStages = 2;
 constexpr int kThreads = 192;
 
 struct __align__(8) AttnBars {
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], k_rot[kStages];
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, pv_done, q_ready, mma_done;
+  uint64_t p_full, pv_done, q_full, q_ready, mma_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -88,7 +94,7 @@ template <int D, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                 const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
-                const AttnParams p) {
+                const __grid_constant__ CUtensorMap map_q, const AttnParams p) {
   using SM = AttnSmem<D, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->k_rot[s], 128);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -118,14 +123,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->p_full, 128);
     mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_ready, 128);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
+    if (my_nt > 0) {
+      // raw Q rows of the G heads, head-major ({64, R, G, 1} boxes; rows past
+      // the chunk arrive as zeros); RoPE is applied in place below
+      prefetch_tensormap(&map_q);
+      mbar_arrive_expect_tx(&bars->q_full, static_cast<uint32_t>(D * p.R * p.G * 2));
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d(smem + SM::kQ + blk * kBM * 128, &map_q, &bars->q_full, blk * 64, qt * p.R, kvh * p.G, b);
+    }
     if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P) && kvh == 0 && blockIdx.x == 0)
       set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
     if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C) && kvh == 0 && blockIdx.x == 0)
       set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  }
+  // Softmax threads: table values of their first Q items, loaded while the
+  // barriers, tensor memory and the Q copy are being set up.  An item is one
+  // (chunk row, 8-dim chunk pair); its table values serve all G heads.
+  constexpr int kQT = 4;  // items per thread whose tables are held at once
+  const int q_items = p.R * (D / 16);
+  RopeTab qtab[kQT];
+  if (warp >= 2 && my_nt > 0) {
+#pragma unroll
+    for (int u = 0; u < kQT; ++u) {
+      const int item = (threadIdx.x - 64) + 128 * u;
+      const int il = item / (D / 16), kc = item % (D / 16);
+      const int ri = qt * p.R + il;
+      if (item < q_items && ri < p.C) {
+        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
+        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
+        qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -148,12 +182,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&map_kn);
       prefetch_tensormap(&map_vn);
       int issued = 0;
+      bool waited_keys = false;
       for (int q = 0; q < my_nt; ++q) {
         const int st = q % kStages;
         if (!mbar_wait(&bars->kv_empty[st], ((q / kStages) + 1) & 1, abort)) break;
         const int j = tp.index(q);
         const bool chunk = j < tp.Tc;
         const int base = (chunk ? j : j - tp.Tc) * BN;
+        if (chunk && !waited_keys) {
+          grid_dependency_wait();  // rotated chunk keys are written by the preceding grid
+          waited_keys = true;
+        }
         const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
         const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
         mbar_arrive_expect_tx(&bars->k_full[st], SM::kKBytes);
@@ -201,8 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; ok && q < my_nt; ++q) {
         const int st = q % kStages;
         const int sb = q & 1;
-        const bool chunk = tp.index(q) < tp.Tc;
-        ok = mbar_wait(chunk ? &bars->k_rot[st] : &bars->k_full[st], (q / kStages) & 1, abort);
+        ok = mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort);
         if (!ok) break;
         ok = mbar_wait(&bars->s_empty[sb], ((q >> 1) + 1) & 1, abort);
         if (!ok) break;
@@ -234,58 +272,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = g < p.G && i < p.C;
     const int h = kvh * p.G + (valid ? g : 0);
 
-    // Q rows, rotated, into the 128-byte-swizzled K-major operand tile.  An
-    // item is one (chunk row, 8-dim chunk pair, group of four heads): the
-    // heads share the row's table values, loaded once per item.  Each thread
-    // keeps two items' loads in flight before rotating either.
-    {
+    // RoPE on the raw Q rows in shared memory (128-byte-swizzled K-major
+    // operand tile), item by item, every head of the group per item.
+    if (my_nt > 0) {
       const int R = p.R;
-      const int HG = (p.G + 3) / 4;
-      const int n_items = R * (D / 16) * HG;
-      constexpr int kQU = 2;
-      for (int it0 = tid; it0 < n_items; it0 += 128 * kQU) {
-        RopeTab tab[kQU];
-        uint4 lo[kQU][4], hi[kQU][4];
-        int il[kQU], kc[kQU], g0[kQU];
-        bool in[kQU];
+      bool qok = warp_all(mbar_wait(&bars->q_full, 0, abort));
+      for (int it0 = 0; qok && it0 < q_items; it0 += 128 * kQT) {
 #pragma unroll
-        for (int u = 0; u < kQU; ++u) {
-          const int item = it0 + 128 * u;
-          kc[u] = item % (D / 16);
-          const int t = item / (D / 16);
-          g0[u] = (t % HG) * 4;
-          il[u] = t / HG;
-          const int ri = qt * R + il[u];
-          in[u] = item < n_items && ri < p.C;
-          if (in[u]) {
+        for (int u = 0; u < kQT; ++u) {
+          const int item = it0 + tid + 128 * u;
+          const int il = item / (D / 16), kc = item % (D / 16);
+          if (item >= q_items || qt * R + il >= p.C) continue;
+          if (it0 > 0) {
+            const int ri = qt * R + il;
             const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
             const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-            tab[u] = rope_tab(cr + kc[u] * 8, sr + kc[u] * 8, cr + D / 2 + kc[u] * 8, sr + D / 2 + kc[u] * 8);
+            qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
           }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            lo[u][v] = make_uint4(0, 0, 0, 0);
-            hi[u][v] = lo[u][v];
-            const int g = g0[u] + v;
-            if (in[u] && g < p.G) {
-              const size_t rowoff = ((static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * p.C + ri) * D;
-              lo[u][v] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + kc[u] * 8));
-              hi[u][v] = __ldg(reinterpret_cast<const uint4*>(p.q + rowoff + D / 2 + kc[u] * 8));
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kQU; ++u) {
-          if (it0 + 128 * u >= n_items) break;
-          const int kh = kc[u] + D / 16;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int g = g0[u] + v;
-            if (g >= p.G) break;
-            if (in[u]) rope_apply(lo[u][v], hi[u][v], tab[u]);
-            const int r = g * R + il[u];
-            *reinterpret_cast<uint4*>(sQ + (kc[u] / 8) * (kBM * 128) + sw128(r, kc[u] % 8)) = lo[u][v];
-            *reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8)) = hi[u][v];
+          const int kh = kc + D / 16;
+          for (int g = 0; g < p.G; ++g) {
+            const int r = g * R + il;
+            uint4* pl = reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8));
+            uint4* ph = reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8));
+            uint4 lo = *pl, hi = *ph;
+            rope_apply(lo, hi, qtab[u]);
+            *pl = lo;
+            *ph = hi;
           }
         }
       }
@@ -304,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int past_lo = W > 0 ? max(0, tp.L + i - W + 1) : 0;
     const int ch_lo = W > 0 ? max(0, i - W + 1) : 0;
     const int ch_hi = p.causal ? min(tp.n, i + 1) : (W > 0 ? min(tp.n, i + W) : tp.n);
+    const bool mask_vec = (p.P % 4 == 0) && (p.C % 4 == 0);
     const float* mrow = (p.mask && valid)
                             ? p.mask + ((static_cast<size_t>(b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C)
                             : nullptr;
@@ -311,61 +324,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = kMaskedLog2, l_run = 0.f;
     bool ok = true;
     for (int q = 0; q < my_nt; ++q) {
-      const int st = q % kStages;
       const int sb = q & 1;
       const int j = tp.index(q);
       const bool chunk = j < tp.Tc;
       const int base = (chunk ? j : j - tp.Tc) * BN;
-      if (chunk) {
-        // rotate the raw chunk-K tile in place
-        if (!(ok = warp_all(mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort)))) break;
-        uint8_t* kt = sK + st * SM::kKBytes;
-        // KU items per step, their table loads issued together (one where
-        // the 128-key S tile leaves no registers for more)
-        constexpr int KU = BN == 64 ? 2 : 1;
-        for (int item0 = tid; item0 < BN * (D / 16); item0 += 128 * KU) {
-          RopeTab tab[KU];
-          uint4* pl[KU];
-          uint4* ph[KU];
-          bool use[KU];
-#pragma unroll
-          for (int u = 0; u < KU; ++u) {
-            const int item = item0 + 128 * u;
-            const int r = item / (D / 16);
-            const int kc = item % (D / 16);
-            const int t = base + r;
-            use[u] = item < BN * (D / 16) && t < p.C;
-            const int kh = kc + D / 16;
-            pl[u] = reinterpret_cast<uint4*>(kt + (kc / 8) * (BN * 128) + sw128(r, kc % 8));
-            ph[u] = reinterpret_cast<uint4*>(kt + (kh / 8) * (BN * 128) + sw128(r, kh % 8));
-            if (use[u]) {
-              const float* cr = p.cos + (static_cast<size_t>(b) * p.C + t) * D;
-              const float* sr = p.sin + (static_cast<size_t>(b) * p.C + t) * D;
-              tab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < KU; ++u) {
-            if (!use[u]) continue;
-            uint4 lo = *pl[u], hi = *ph[u];
-            rope_apply(lo, hi, tab[u]);
-            *pl[u] = lo;
-            *ph[u] = hi;
-          }
-        }
-        fence_async_smem();
-        mbar_arrive(&bars->k_rot[st]);
-      }
       // Explicit mask values of this tile, loaded before the wait on S so
       // their latency hides behind the product (64-key tiles only: a 128-key
-      // tile has no registers to spare).
+      // tile has no registers to spare).  With P and C multiples of 4 every
+      // 16-byte vector of the row lies wholly inside or outside [0, lim).
       constexpr bool kMaskEarly = BN == 64;
       float mk[kMaskEarly ? BN : 1];
       if (kMaskEarly && mrow) {
         const int lim = chunk ? p.C : p.P;
         const float* mp = mrow + (chunk ? p.P + base : base);
+        if (mask_vec) {
 #pragma unroll
-        for (int e = 0; e < (kMaskEarly ? BN : 1); ++e) mk[e] = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+          for (int e = 0; e < (kMaskEarly ? BN : 4); e += 4) {
+            float4 v = make_float4(-1e30f, -1e30f, -1e30f, -1e30f);
+            if (base + e < lim) v = __ldg(reinterpret_cast<const float4*>(mp + e));
+            mk[e] = v.x;
+            mk[e + 1] = v.y;
+            mk[e + 2] = v.z;
+            mk[e + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < (kMaskEarly ? BN : 1); ++e) mk[e] = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+        }
       }
       if (!(ok = warp_all(mbar_wait(&bars->s_full[sb], (q >> 1) & 1, abort)))) break;
       tc_fence_after();
@@ -386,12 +371,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pastt = !chunk;
         const int lim = pastt ? p.P : p.C;
         const float* mp = mrow + (pastt ? base : p.P + base);
+        if constexpr (kMaskEarly) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          float mv;
-          if constexpr (kMaskEarly) mv = mk[e];
-          else mv = (base + e < lim) ? __ldg(mp + e) : -1e30f;
-          x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(mv, kLog2e));
+          for (int e = 0; e < BN; ++e) x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(mk[e], kLog2e));
+        } else if (mask_vec) {
+#pragma unroll
+          for (int e = 0; e < BN; e += 4) {
+            float4 v = make_float4(-1e30f, -1e30f, -1e30f, -1e30f);
+            if (base + e < lim) v = __ldg(reinterpret_cast<const float4*>(mp + e));
+            x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(v.x, kLog2e));
+            x[e + 1] = __fmaf_rn(x[e + 1], p.sl2, __fmul_rn(v.y, kLog2e));
+            x[e + 2] = __fmaf_rn(x[e + 2], p.sl2, __fmul_rn(v.z, kLog2e));
+            x[e + 3] = __fmaf_rn(x[e + 3], p.sl2, __fmul_rn(v.w, kLog2e));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) {
+            const float mv = (base + e < lim) ? __ldg(mp + e) : -1e30f;
+            x[e] = __fmaf_rn(x[e], p.sl2, __fmul_rn(mv, kLog2e));
+          }
         }
       } else {
         const int lo = (chunk ? ch_lo : past_lo) - base;
@@ -630,6 +628,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // This grid completes only after the key pre-pass has (stream order for
+  // whatever follows).
+  if (threadIdx.x == 0) grid_dependency_wait();
+}
+
+// Rotated chunk keys for the single-tile kernel: one thread per (row, 8-dim
+// chunk pair), the append's fp32 arithmetic.  It lets the dependent attention
+// grid start at once.
+__global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
+  grid_launch_dependents();
+  const int D = p.D;
+  const int HP = D / 16;
+  const long long total = static_cast<long long>(p.B) * p.Hkv * p.C * HP;
+  for (long long it = blockIdx.x * 256LL + threadIdx.x; it < total; it += static_cast<long long>(gridDim.x) * 256) {
+    const int kc = static_cast<int>(it % HP);
+    const long long r = it / HP;  // row of [B, Hkv, C]
+    const int i = static_cast<int>(r % p.C);
+    const int b = static_cast<int>(r / p.C / p.Hkv);
+    const uint16_t* src = p.k_new + r * D;
+    uint4 lo = __ldg(reinterpret_cast<const uint4*>(src + kc * 8));
+    uint4 hi = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
+    const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
+    const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
+    rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    uint16_t* dst = p.k_rot + r * D;
+    *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
+    *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
+  }
 }
 
 // Merge split-KV partials in fixed split order: one warp per output row.
@@ -694,23 +720,30 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
     attr_set = true;
   }
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
+  const long long items = static_cast<long long>(p.B) * p.Hkv * p.C * (D / 16);
+  const int kblocks = static_cast<int>(max(1LL, min(static_cast<long long>(152) * 8, (items + 255) / 256)));
+  rope_chunk_k_kernel<<<kblocks, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SM::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
   if (p.cluster) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SM::kAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], p);
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
   }
-  kern<<<grid, kThreads, SM::kAlloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  return cudaGetLastError();
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
 // Whether clusters of `splits` CTAs of attn_kernel<D, BN> fit on the device.

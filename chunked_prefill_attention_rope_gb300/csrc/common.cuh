@@ -311,6 +311,18 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ dependent launches
+
+// Lets the grid launched after this one (as a programmatic dependent) start.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grid this one depends on has completed and its writes are
+// visible (returns at once when launched without a programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ barriers, clusters
 
 // Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.

@@ -66,7 +66,8 @@ inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >
 inline bool attn_uses_decode(int D, int C, int G) { return C == 1 && (D == 64 || D == 128) && G <= 16; }
 cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 // maps: cache K, cache V (dims {D, P, Hkv, B}), chunk K, chunk V (dims {D, C, Hkv, B}),
-// all bf16, box {64, block_n, 1, 1}, 128-byte swizzle.
+// all bf16, box {64, block_n, 1, 1}, 128-byte swizzle; for the single-tile
+// kernel also raw Q (dims {D, C, Hq, B}, box {64, R, G, 1}).
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
 
 struct CacheView {
