@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
 
+  grid_launch_dependents();  // combine_kernel (if any) may be scheduled now; it waits for this grid
   const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
   const int my_nt = tp.count();
 
@@ -660,6 +661,7 @@ __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
 
 // Merge split-KV partials in fixed split order: one warp per output row.
 __global__ void combine_kernel(const AttnParams p) {
+  grid_dependency_wait();  // partials of the attention grid before it
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   const int rows = p.B * p.Hq * p.C;
@@ -778,8 +780,7 @@ static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
   const int rows = p.B * p.Hq * p.C;
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
-  combine_kernel<<<blocks, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(combine_kernel, dim3(blocks), dim3(threads), 0, stream, p);
 }
 
 int attn_block_n(int D) { return D == 256 ? 64 : 128; }

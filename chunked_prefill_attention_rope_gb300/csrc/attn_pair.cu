@@ -231,6 +231,7 @@ __device__ void plan_units(const AttnParams& p) {
 // issued together.  A warp covers four consecutive rows of each head, so
 // every load and store is a contiguous 512-byte run per head.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) {
+  grid_launch_dependents();
   if (blockIdx.x == gridDim.x - 1) {
     plan_units(p);
     return;
@@ -322,6 +323,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     tmem_relinquish();
   }
   __syncthreads();
+  // the merge grid may be scheduled now; this grid's inputs (plan, rotated
+  // Q and keys) come from prep_kernel, launched just before it
+  grid_launch_dependents();
+  grid_dependency_wait();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   uint8_t* sK = smem + CF::kK;
@@ -702,6 +707,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnPa
   const int unit = blockIdx.x;
   const Unit x = unit_of(p, unit);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  grid_dependency_wait();  // partials and tags of attn_pair_kernel
   if (warp == 0) {
     const int gblk = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
     const int member = x.pair % p.team;
@@ -856,9 +862,13 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
   const int rope_blocks =
       static_cast<int>(max(1LL, min(static_cast<long long>(65535) * 4, (items + kPrepThreads - 1) / kPrepThreads)));
   prep_kernel<<<rope_blocks + 1, kPrepThreads, 0, stream>>>(p);
-  kern<<<p.ctas, kThreadsPair, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  merge_units_kernel<D><<<dim3(p.units, kUnitRows / kMergeRows), kMergeThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(kern, dim3(p.ctas), dim3(kThreadsPair), smem, stream, maps[0], maps[1], maps[2], maps[3],
+                       maps[4], p);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(merge_units_kernel<D>, dim3(p.units, kUnitRows / kMergeRows), dim3(kMergeThreads), 0,
+                          stream, p);
 }
 
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {

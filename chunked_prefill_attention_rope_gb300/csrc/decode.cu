@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
                        const AttnParams p) {
   using CF = DecCfg<D>;
   constexpr int NS = CF::kStages;
+  grid_launch_dependents();  // combine_kernel may be scheduled now; it waits for this grid
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NB = D / 8;   // n-blocks of O
   extern __shared__ uint8_t smem_raw[];

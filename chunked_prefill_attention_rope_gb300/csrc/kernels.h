@@ -7,6 +7,25 @@
 
 namespace cpa {
 
+// Launch `kern` as a programmatic dependent of the grid before it on the
+// stream: it may start while that grid runs and must call
+// grid_dependency_wait() before reading that grid's results.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct AttnParams {
   int B, Hq, Hkv, D, C, P, G, R, nq, splits;
   float sl2;  // softmax scale * log2(e)
