@@ -533,6 +533,14 @@ def measure_page1(cpa, dev, reps=10):
                                    workspace=ws, err=err)
             cpa.kv_append(cache, inp["k"], inp["v"], cos, sin, n_real, err=err)
 
+    def run_fused():
+        for kind, inp, cache, out, sel in layers:
+            mask, cos, sin = shared[kind]
+            cache.len.copy_(len0)
+            cpa.chunk_prefill_attn_append(inp["q"], inp["k"], inp["v"], cos, sin, cache, w.P, n_real,
+                                          past_len=len0, n_real=n_real, mask=mask, sel_row=sel_row, out=out,
+                                          out_sel=sel, workspace=ws, err=err)
+
     for _ in range(3):
         run()
     torch.cuda.synchronize()
@@ -546,12 +554,15 @@ def measure_page1(cpa, dev, reps=10):
         ts.append(a.elapsed_time(b) * 1e3)
     eager = statistics.median(ts)
     graph = _graph_us(run, reps)
+    graph_fused = _graph_us(run_fused, reps)
     if int(err[0]) != 0:
         raise RuntimeError(f"page-1 shape: device error bits {int(err[0])}")
     return {"workload": "page-1 call shape: 18 layers x (attention with explicit mask + select, global append); "
                         "B1, 4/1 heads, D256, past 800, C64 (52 real)",
             "eager_us_per_layer": round(eager / w.layers, 2), "graph_us_per_layer": round(graph / w.layers, 2),
-            "timing": "CUDA events, median of 10; graph = the 18 layers captured once and replayed; L2-resident"}
+            "graph_us_per_layer_fused_append": round(graph_fused / w.layers, 2),
+            "timing": "CUDA events, median of 10; graph = the 18 layers captured once and replayed; L2-resident; "
+                      "fused = chunk_prefill_attn_append instead of attention + kv_append"}
 
 
 # ------------------------------------------------------------------ oracle arm

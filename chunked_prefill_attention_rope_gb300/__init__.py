@@ -6,6 +6,8 @@ library has not been built.  torch supplies device memory and the current
 stream.  The entry points mirror include/cpa.h:
 
     chunk_prefill_attn   one chunk of C rows against the KV cache
+    chunk_prefill_attn_append
+                         the same, and the chunk appended to a global cache
     decode_step          the C = 1 case
     kv_append            append the chunk (rotated K, V) to the cache
     kv_snapshot_padded_append / kv_rollback_padded_append
@@ -23,7 +25,7 @@ import torch
 
 __all__ = [
     "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
-    "decode_step",
+    "decode_step", "chunk_prefill_attn_append",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
     "attn_workspace_size", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
     "tail_plan", "TAIL_SCALAR", "TAIL_PADDED", "TAIL_AUTO", "TAIL_FORCE_SCALAR", "TAIL_FORCE_PADDED",
@@ -83,6 +85,7 @@ def load_library():
     lib.cpa_chunk_prefill_attn.argtypes = [ctypes.POINTER(_AttnArgs), vp]
     lib.cpa_decode_step.argtypes = [ctypes.POINTER(_AttnArgs), vp]
     lib.cpa_chunk_prefill_attn_noalloc.argtypes = [ctypes.POINTER(_AttnArgs), vp]
+    lib.cpa_chunk_prefill_attn_append.argtypes = [ctypes.POINTER(_AttnArgs), vp, vp]
     lib.cpa_attn_workspace_size.argtypes = [i32] * 6
     lib.cpa_attn_workspace_size.restype = sz
     lib.cpa_kv_append.argtypes = [ctypes.POINTER(_Cache), vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, sz, vp, vp]
@@ -94,7 +97,8 @@ def load_library():
     lib.cpa_status_str.argtypes = [i32]
     lib.cpa_status_str.restype = ctypes.c_char_p
     lib.cpa_version.restype = ctypes.c_char_p
-    for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_chunk_prefill_attn_noalloc", "cpa_kv_append",
+    for f in ("cpa_chunk_prefill_attn", "cpa_decode_step", "cpa_chunk_prefill_attn_noalloc",
+              "cpa_chunk_prefill_attn_append", "cpa_kv_append",
               "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append", "cpa_tail_plan"):
         getattr(lib, f).restype = i32
     _LIB = lib
@@ -162,7 +166,7 @@ def cache_scratch_size(cache: KVCache, C: int) -> int:
 def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
           window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
           out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None,
-          alloc_workspace: bool = True):
+          alloc_workspace: bool = True, append_rows=None):
     lib = load_library()
     B, Hq, C, D = q.shape
     Hkv = k_new.shape[1]
@@ -192,7 +196,11 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
                   _ptr(n_real), int(window), 1 if causal else 0, _ptr(sel_row), out.data_ptr(),
                   _ptr(out_sel), _ptr(workspace), 0 if workspace is None else workspace.numel(),
                   err.data_ptr())
-    _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream)))
+    if append_rows is not None:
+        _need(append_rows, "n_rows", torch.int32, (B,))
+        _check(getattr(lib, entry)(ctypes.byref(a), append_rows.data_ptr(), _stream(stream)))
+    else:
+        _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream)))
     return out, out_sel
 
 
@@ -210,6 +218,13 @@ def chunk_prefill_attn_noalloc(q, k_new, v_new, cos, sin, cache: KVCache, P: int
     kw["workspace"] = None
     return _attn("cpa_chunk_prefill_attn_noalloc", q, k_new, v_new, cos, sin, cache, P,
                  alloc_workspace=False, **kw)
+
+
+def chunk_prefill_attn_append(q, k_new, v_new, cos, sin, cache: KVCache, P: int, n_rows, **kw):
+    """chunk_prefill_attn then kv_append(cache, k_new, v_new, cos, sin, n_rows) in one
+    call (cpa_chunk_prefill_attn_append): the RoPE pre-pass writes the new cache rows,
+    len advances after the attention.  GLOBAL caches only."""
+    return _attn("cpa_chunk_prefill_attn_append", q, k_new, v_new, cos, sin, cache, P, append_rows=n_rows, **kw)
 
 
 def decode_step(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):

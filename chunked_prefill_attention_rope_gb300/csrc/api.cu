@@ -153,7 +153,7 @@ CacheView view_of(const cpa_cache* c) {
   return v;
 }
 
-cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
+cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, const int32_t* app_n = nullptr) {
   if (!a) return CPA_ERR_NULL;
   if (!a->q || !a->k_new || !a->v_new || !a->cos || !a->sin || !a->out || !a->err) return CPA_ERR_NULL;
   if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->C < 1 || a->P < 0) return CPA_ERR_SHAPE;
@@ -217,6 +217,17 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
   p.out_sel = a->out_sel;
   p.err = a->err;
   p.k_new = static_cast<const uint16_t*>(a->k_new);
+  p.v_new = static_cast<const uint16_t*>(a->v_new);
+  if (app_n && g.path != kPathDecode) {
+    p.app_n = app_n;
+    p.app_k = static_cast<uint16_t*>(c->k);
+    p.app_v = static_cast<uint16_t*>(c->v);
+    p.app_sb = c->stride_b;
+    p.app_sh = c->stride_h;
+    p.app_ss = c->stride_s;
+    p.app_len = c->len;
+    p.app_cap = c->cap;
+  }
   if (g.path == kPathPair) {
     const PairTeams& t = g.teams;
     p.pairs = t.pairs;
@@ -254,7 +265,20 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode) {
         !make_map(&maps[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn))
       return CPA_ERR_CUDA;
   }
-  return launch_attn(maps, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+  if (launch_attn(maps, p, stream) != cudaSuccess) return CPA_ERR_CUDA;
+  if (app_n) {
+    // the rows were written by the RoPE pre-pass; advance len after the
+    // attention (one token: the separate append kernels after the attention)
+    const cudaError_t e =
+        g.path == kPathDecode
+            ? launch_global_append(view_of(c), ChunkView{static_cast<const uint16_t*>(a->k_new),
+                                                         static_cast<const uint16_t*>(a->v_new), a->cos, a->sin,
+                                                         app_n},
+                                   a->B, a->Hkv, a->D, a->C, a->err, stream)
+            : launch_fused_append_len(p, stream);
+    if (e != cudaSuccess) return CPA_ERR_CUDA;
+  }
+  return CPA_OK;
 }
 
 cpa_status chunk_check(const void* k_new, const void* v_new, const float* cos, const float* sin,
@@ -277,6 +301,13 @@ cpa_status cpa_chunk_prefill_attn(const cpa_attn_args* args, cpa_stream stream) 
 
 cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream) {
   return attn_impl(args, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+cpa_status cpa_chunk_prefill_attn_append(const cpa_attn_args* args, const int32_t* n_rows, cpa_stream stream) {
+  if (!args || !n_rows) return CPA_ERR_NULL;
+  if (args->cache && args->cache->kind != CPA_CACHE_GLOBAL) return CPA_ERR_UNSUPPORTED;
+  if (!aligned16(n_rows)) return CPA_ERR_ALIGN;
+  return attn_impl(args, reinterpret_cast<cudaStream_t>(stream), false, n_rows);
 }
 
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P) {

@@ -190,8 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = tp.index(q);
         const bool chunk = j < tp.Tc;
         const int base = (chunk ? j : j - tp.Tc) * BN;
-        if (chunk && !waited_keys) {
-          grid_dependency_wait();  // rotated chunk keys are written by the preceding grid
+        if ((chunk || p.app_n) && !waited_keys) {
+          // rotated chunk keys (and, with a fused append, new cache rows) are
+          // written by the preceding grid
+          grid_dependency_wait();
           waited_keys = true;
         }
         const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
@@ -656,7 +658,14 @@ __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
     uint16_t* dst = p.k_rot + r * D;
     *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
     *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
+    if (p.app_n) fused_append_pair(p, b, static_cast<int>((r / p.C) % p.Hkv), i, kc, lo, hi);
   }
+}
+
+// Fused append's length update, after the attention grid (and its merge).
+__global__ void fused_len_kernel(const AttnParams p) {
+  grid_dependency_wait();
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) fused_append_len(p, b);
 }
 
 // Merge split-KV partials in fixed split order: one warp per output row.
@@ -784,6 +793,10 @@ static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
 }
 
 int attn_block_n(int D) { return D == 256 ? 64 : 128; }
+
+cudaError_t launch_fused_append_len(const AttnParams& p, cudaStream_t stream) {
+  return launch_dependent(fused_len_kernel, dim3(1), dim3(256), 0, stream, p);
+}
 
 bool attn_cluster_ok(int D, int splits) {
   if (splits < 2 || splits > kMaxClusterSplits) return false;

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) 
       uint16_t* dst = (hh < p.Hq ? p.q_rot : p.k_rot) + off[u];
       *reinterpret_cast<uint4*>(dst + kc * 8) = lo[u];
       *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi[u];
+      if (p.app_n && hh >= p.Hq) fused_append_pair(p, b, hh - p.Hq, i, kc, lo[u], hi[u]);
     }
   }
 }
@@ -708,6 +709,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnPa
   const Unit x = unit_of(p, unit);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   grid_dependency_wait();  // partials and tags of attn_pair_kernel
+  if (p.app_n && blockIdx.x == 0 && blockIdx.y == 0)  // fused append: every reader of len is done
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) fused_append_len(p, b);
   if (warp == 0) {
     const int gblk = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
     const int member = x.pair % p.team;

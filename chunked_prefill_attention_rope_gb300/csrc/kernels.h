@@ -57,7 +57,18 @@ struct AttnParams {
   int32_t* ptag;          // [2 * ctas] unit of each CTA's partial slots (-1: none)
   int cluster;            // single-tile path: the splits of a query tile form one
                           // thread-block cluster and merge their partials in-kernel
+  // Fused global append (app_n non-null): the rotated chunk keys and the
+  // values of rows [0, n_b) go to cache slots [len_b, len_b + n_b) from the
+  // RoPE pre-pass; len is advanced after the attention has read it.
+  const uint16_t* v_new;  // chunk values [B, Hkv, C, D]
+  const int32_t* app_n;   // [B] rows to append, or null
+  uint16_t* app_k;
+  uint16_t* app_v;
+  int64_t app_sb, app_sh, app_ss;  // cache strides in elements
+  int32_t* app_len;
+  int app_cap;
 };
+
 
 // Team-aligned stream-K layout for these sizes, and its workspace.
 struct PairTeams {
@@ -88,6 +99,8 @@ cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cud
 // all bf16, box {64, block_n, 1, 1}, 128-byte swizzle; for the single-tile
 // kernel also raw Q (dims {D, C, Hq, B}, box {64, R, G, 1}).
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);
+// Fused append's length update as a programmatic dependent of the attention.
+cudaError_t launch_fused_append_len(const AttnParams& p, cudaStream_t stream);
 
 struct CacheView {
   uint16_t* k;

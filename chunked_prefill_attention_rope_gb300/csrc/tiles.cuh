@@ -90,4 +90,34 @@ struct RowSpan {
   }
 };
 
+// Fused append, device side: write rotated key chunk pair (lo, hi) and the
+// value chunks of chunk row i of (b, kv head h) into the cache, if the
+// sequence has room (len + n <= cap) and i < n.
+__device__ __forceinline__ void fused_append_pair(const AttnParams& p, int b, int h, int i, int kc,
+                                                  uint4 lo, uint4 hi) {
+  const int n = min(max(p.app_n[b], 0), p.C);
+  const int L = p.app_len[b];
+  if (L < 0 || L + n > p.app_cap || i >= n) return;
+  const int D = p.D;
+  const size_t dst = static_cast<size_t>(b) * p.app_sb + static_cast<size_t>(h) * p.app_sh +
+                     static_cast<size_t>(L + i) * p.app_ss;
+  const size_t src = ((static_cast<size_t>(b) * p.Hkv + h) * p.C + i) * D;
+  *reinterpret_cast<uint4*>(p.app_k + dst + kc * 8) = lo;
+  *reinterpret_cast<uint4*>(p.app_k + dst + D / 2 + kc * 8) = hi;
+  *reinterpret_cast<uint4*>(p.app_v + dst + kc * 8) = *reinterpret_cast<const uint4*>(p.v_new + src + kc * 8);
+  *reinterpret_cast<uint4*>(p.app_v + dst + D / 2 + kc * 8) =
+      *reinterpret_cast<const uint4*>(p.v_new + src + D / 2 + kc * 8);
+}
+
+// Fused append: advance len (or flag the sequence that has no room); one
+// thread per sequence, after every reader of len.
+__device__ __forceinline__ void fused_append_len(const AttnParams& p, int b) {
+  const int raw = p.app_n[b];
+  const int n = min(max(raw, 0), p.C);
+  if (raw != n) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  const int L = p.app_len[b];
+  if (L >= 0 && L + n <= p.app_cap) p.app_len[b] = L + n;
+  else set_err(p.err, CPA_EBIT_CAPACITY);
+}
+
 }  // namespace cpa

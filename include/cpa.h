@@ -207,6 +207,28 @@ cpa_status cpa_kv_append(const cpa_cache* cache, const void* k_new, const void* 
                          int B, int Hkv, int D, int C,
                          void* scratch, size_t scratch_bytes, int32_t* err, cpa_stream stream);
 
+/*
+ * Attention and global append in one call ([P1, Change]: "K/V extended by
+ * the chunk"; [P2, Runtime behavior]: the runtime writes the new K/V into its
+ * buffers after the step).  Same results as cpa_chunk_prefill_attn(args)
+ * followed by cpa_kv_append(args->cache, args->k_new, args->v_new, args->cos,
+ * args->sin, n_rows, ...): identical outputs, identical cache bytes in rows
+ * [0, len) and len, identical error bits.  The RoPE pre-pass that rotates
+ * the chunk keys for the attention also writes them (and the values) to the
+ * cache slots [len_b, len_b + n_b), and len advances once the attention has
+ * read it, so the keys are rotated once and the append costs no extra pass.
+ *   n_rows   device int32 [B], 16-byte aligned: rows to append (as
+ *            cpa_kv_append's n_rows).
+ * The cache must be GLOBAL (CPA_ERR_UNSUPPORTED otherwise: a sliding append
+ * evicts rows the attention reads; use the separate calls).  The new rows are
+ * written before the attention reads the cache, into slots the attention
+ * does not see when past_len <= len (always with the implicit mask; an
+ * explicit mask must keep slots >= len masked, as it must for dead rows).
+ * One-token chunks run the attention and then the separate append kernels.
+ * Errors as cpa_chunk_prefill_attn and cpa_kv_append.
+ */
+cpa_status cpa_chunk_prefill_attn_append(const cpa_attn_args* args, const int32_t* n_rows, cpa_stream stream);
+
 /* Scratch bytes a SLIDING cache needs for cpa_kv_append and the padded-append
  * snapshot / rollback with chunk size C (0 for a GLOBAL cache). */
 size_t cpa_cache_scratch_size(const cpa_cache* cache, int B, int Hkv, int D, int C);

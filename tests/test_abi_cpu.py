@@ -26,7 +26,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     _, so = lib
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     for name in names:
         assert hasattr(so, name), name
 
