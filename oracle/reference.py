@@ -83,7 +83,7 @@ def rope_rotate(x_bits, cos, sin) -> np.ndarray:
 
 # ---------------------------------------------------------------- masks
 
-def visible(L: int, n: int, C: int, P: int, window: int, causal: int) -> np.ndarray:
+def visible(L: int, n: int, C: int, P: int, window: int, causal: int, sink: int = 0) -> np.ndarray:
     """Boolean [C, P+C]: which key columns query row i may attend to.
 
     [P1, Change]: the mask carries the causal band inside the chunk, the zero
@@ -91,6 +91,14 @@ def visible(L: int, n: int, C: int, P: int, window: int, causal: int) -> np.ndar
     packed into the first past_len slots; unfilled slots stay masked; the
     current token is visible.  Query row i sits at position L + i; past slot j
     at position j; chunk row t at position L + t.
+
+    Sinks ("Pad the chunked-prefill tail for sliding-window models", Fix and
+    review: the sliding cache keeps S pinned sink rows in slots [0, S) and
+    compacts the rest chronologically).  Reading: the pinned rows are visible
+    to every query row whatever the window; a non-sink slot j holds the token
+    L - j rows before the chunk (compaction keeps the newest rows contiguous
+    and ending at slot L - 1), so the window rule on L + i - j applies to it
+    unchanged.  sink = 0 is the plain rule.
     """
     i = np.arange(C)[:, None]
     pos_q = L + i
@@ -101,15 +109,15 @@ def visible(L: int, n: int, C: int, P: int, window: int, causal: int) -> np.ndar
     if causal:
         chunk = chunk & (t <= i)
     if window > 0:
-        past = past & (np.abs(pos_q - j) < window)
+        past = past & ((np.abs(pos_q - j) < window) | (j < sink))
         chunk = chunk & (np.abs(pos_q - (L + t)) < window)
     return np.concatenate([np.broadcast_to(past, (C, P)),
                            np.broadcast_to(chunk, (C, C))], axis=1)
 
 
-def explicit_mask(L: int, n: int, C: int, P: int, window: int, causal: int) -> np.ndarray:
+def explicit_mask(L: int, n: int, C: int, P: int, window: int, causal: int, sink: int = 0) -> np.ndarray:
     """The additive fp32 mask [C, P+C] a caller builds: 0 = attend, -1e30 = masked [P1]."""
-    return np.where(visible(L, n, C, P, window, causal), np.float32(0.0),
+    return np.where(visible(L, n, C, P, window, causal, sink), np.float32(0.0),
                     np.float32(MASKED)).astype(np.float32)
 
 
@@ -140,7 +148,7 @@ def attend(q, keys, values, add_mask, scale: float) -> np.ndarray:
 
 
 def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, n_real,
-                       window=0, causal=1, mask=None, scale=None, sel_row=None):
+                       window=0, causal=1, mask=None, scale=None, sel_row=None, sink=0):
     """One chunk of C rows attending over P cached slots plus the chunk itself.
 
     [P1, Change]: heads-first [heads, C, headDim] Q/K/V, RoPE from the cos/sin
@@ -150,7 +158,7 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
 
     q [B,Hq,C,D], k_new/v_new [B,Hkv,C,D], cache_k/cache_v [B,Hkv,>=P,D]: bf16 bits.
     cos/sin [B,C,D] fp32.  mask: None (implicit from past_len, n_real, window,
-    causal) or fp32 [B,Hq,C,P+C].  Returns (out fp64 [B,Hq,C,D],
+    causal, sink) or fp32 [B,Hq,C,P+C].  Returns (out fp64 [B,Hq,C,D],
     out_sel fp64 [B,Hq*D] or None).
     """
     q = np.asarray(q)
@@ -166,7 +174,7 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
     out = np.zeros((B, Hq, C, D), dtype=np.float64)
     for b in range(B):
         L, n = int(past_len[b]), int(n_real[b])
-        implicit = None if mask is not None else explicit_mask(L, n, C, P, window, causal)
+        implicit = None if mask is not None else explicit_mask(L, n, C, P, window, causal, sink)
         for h in range(Hq):
             kvh = h // G
             keys = np.concatenate([bf16_to_f32(cache_k[b, kvh, :P]).astype(np.float64),
@@ -181,7 +189,7 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
     return out, out_sel
 
 
-def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window=0):
+def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window=0, sink=0):
     """One-token decode: the C = 1 case.
 
     [P2, Mask/cache layout]: the mask unmasks the valid past slots and the
@@ -190,7 +198,7 @@ def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window
     B = np.asarray(q).shape[0]
     ones = np.ones(B, dtype=np.int64)
     out, _ = chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P,
-                                past_len, ones, window=window, causal=0)
+                                past_len, ones, window=window, causal=0, sink=sink)
     return out
 
 

@@ -10,7 +10,9 @@
 (c) the explicit per-head mask and the implicit (past_len, n_real, window,
     causal) description give the same result.
     plus: a sliding cache fed by exact appends holds the sinks and then the
-    newest rows in order (closed form, independent of the compaction code).
+    newest rows in order (closed form, independent of the compaction code);
+    and the implicit mask's slot -> position reading with sinks agrees with
+    the absolute positions the sliding cache actually stores.
 """
 import numpy as np
 import pytest
@@ -129,6 +131,50 @@ def test_sliding_closed_form_sinks_then_newest():
         assert int(length[0]) == len(keep)
         assert np.array_equal(ck[0, 0, :len(keep)], k[0, 0, keep])
         assert np.array_equal(cv[0, 0, :len(keep)], v[0, 0, keep])
+
+
+@pytest.mark.parametrize("W,S", [(10, 0), (10, 2), (12, 3), (7, 1)])
+def test_sink_mask_matches_positions_in_the_sliding_cache(W, S):
+    """The implicit mask with sinks, against brute force over absolute positions.
+
+    The cache is fed by the oracle's own sliding append with each row's token
+    position stored in its V bits; before every chunk the mask from visible()
+    must equal: pinned sink slot (j < S), or a token within the window of the
+    query's position; chunk keys causal and within the window."""
+    D = 4
+    T = 60
+    zc = np.ones((1, 16, D), np.float32); zs = np.zeros((1, 16, D), np.float32)
+    ck = np.zeros((1, 1, W, D), dtype=np.uint16); cv = np.zeros_like(ck)
+    length = np.zeros(1, dtype=np.int64)
+    s = 0
+    for n in [3, 1, 4, 6, 2, 6, 5, 1, 6, 3, 6, 4, 6, 2]:
+        if n > W - S:
+            n = W - S
+        C = 6
+        L = int(length[0])
+        pos_slot = cv[0, 0, :L, 0].astype(np.int64)          # absolute positions in the cache
+        vis = O.visible(L, n, C, W, W, 1, S)                 # P = W slot columns
+        for i in range(C):
+            pos_q = s + i
+            for j in range(W):
+                want = j < L and (j < S or pos_q - pos_slot[j] < W)
+                assert bool(vis[i, j]) == want, (W, S, s, i, j)
+            for t in range(C):
+                want = t < n and t <= i and (i - t) < W
+                assert bool(vis[i, W + t]) == want, (W, S, s, i, t)
+        newk = np.zeros((1, 1, n, D), np.uint16)
+        newv = np.zeros((1, 1, n, D), np.uint16)
+        newv[0, 0, :, 0] = np.arange(s, s + n)
+        O.kv_append_sliding(ck, cv, length, newk, newv, zc[:, :n], zs[:, :n], [n], W, S)
+        s += n
+        if s >= T:
+            break
+    assert s > 2 * W   # eviction happened many times
+
+
+def test_sink_zero_is_the_plain_mask():
+    for L, n, C, P, W in [(5, 3, 4, 8, 4), (8, 4, 4, 8, 3), (0, 4, 4, 6, 2)]:
+        assert np.array_equal(O.visible(L, n, C, P, W, 1, 0), O.visible(L, n, C, P, W, 1))
 
 
 @pytest.mark.parametrize("S", [0, 2])
