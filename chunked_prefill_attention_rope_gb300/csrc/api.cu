@@ -164,10 +164,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   const cpa_status cs = check_cache(a->cache, a->D);
   if (cs != CPA_OK) return cs;
   if (a->P > a->cache->cap) return CPA_ERR_SHAPE;
-  if (!a->mask) {
-    if (!a->past_len || !a->n_real) return CPA_ERR_NULL;
-    if (a->cache->kind == CPA_CACHE_SLIDING && a->cache->sink > 0) return CPA_ERR_UNSUPPORTED;
-  }
+  if (!a->mask && (!a->past_len || !a->n_real)) return CPA_ERR_NULL;
   if (a->out_sel && !a->sel_row && !a->n_real) return CPA_ERR_NULL;
   if (!aligned16(a->q) || !aligned16(a->k_new) || !aligned16(a->v_new) || !aligned16(a->cos) ||
       !aligned16(a->sin) || !aligned16(a->out) || (a->out_sel && !aligned16(a->out_sel)) ||
@@ -213,6 +210,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.sel_row = a->sel_row;
   p.window = a->window;
   p.causal = a->causal ? 1 : 0;
+  p.sink = (!a->mask && a->cache->kind == CPA_CACHE_SLIDING) ? a->cache->sink : 0;
   p.out = static_cast<uint16_t*>(a->out);
   p.out_sel = a->out_sel;
   p.err = a->err;

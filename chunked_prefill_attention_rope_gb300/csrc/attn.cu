@@ -397,8 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const int lo = (chunk ? ch_lo : past_lo) - base;
         const int hi = valid ? ((chunk ? ch_hi : tp.L) - base) : -1;
+        const int sk = (valid && !chunk) ? min(p.sink, tp.L) - base : 0;  // pinned sink slots
 #pragma unroll
-        for (int e = 0; e < BN; ++e) x[e] = (e >= lo && e < hi) ? __fmul_rn(x[e], p.sl2) : kMaskedLog2;
+        for (int e = 0; e < BN; ++e)
+          x[e] = ((e >= lo && e < hi) || e < sk) ? __fmul_rn(x[e], p.sl2) : kMaskedLog2;
       }
       float mt = x[0];
 #pragma unroll

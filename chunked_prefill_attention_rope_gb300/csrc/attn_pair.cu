@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         const int t = tp.index(a + jj);
         const bool chunk = t < tp.Tc;
         const int base = (chunk ? t : t - tp.Tc) * kBN;
-        int lo, hi;
-        span.tile(chunk, base, lo, hi);
+        int lo, hi, sk;
+        span.tile(chunk, base, lo, hi, sk);
         const float* mp = nullptr;
         int lim = 0;
         if (EXPLICIT) {
@@ -532,8 +532,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 #pragma unroll
           for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
           if (__any_sync(0xffffffffu, lo > 0 || hi < kBN)) {
+            if (!__any_sync(0xffffffffu, sk > 0)) {
 #pragma unroll
-            for (int q = 0; q < kBN; ++q) sc[q] = (q >= lo && q < hi) ? sc[q] : -INFINITY;
+              for (int q = 0; q < kBN; ++q) sc[q] = (q >= lo && q < hi) ? sc[q] : -INFINITY;
+            } else {
+              // pinned sink slots: visible keys [0, sk) and [lo, hi), as one
+              // 32-bit visibility word per 32 keys
+#pragma unroll
+              for (int c = 0; c < kBN / 32; ++c) {
+                const uint32_t vis = bit_range(lo - 32 * c, hi - 32 * c) | bit_range(-32, sk - 32 * c);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) sc[32 * c + q] = ((vis >> q) & 1u) ? sc[32 * c + q] : -INFINITY;
+              }
+            }
           }
           float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll

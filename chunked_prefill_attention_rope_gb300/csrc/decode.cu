@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
   const int W = p.window;
   const int L = tp.L;
   const int past_lo = W > 0 ? max(0, L - W + 1) : 0;
+  const int sinkL = min(p.sink, L);  // pinned sink slots stay visible
   const float* mrow[2] = {nullptr, nullptr};
   if (EXPLICIT) {
 #pragma unroll
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
             v = __fmaf_rn(sv, sl2, __fmul_rn(mv, kLog2e));
             x[nb][2 * hf + e] = v;
           } else {
-            const bool vis = chunk ? (key < tp.n) : (key >= past_lo && key < L);
+            const bool vis = chunk ? (key < tp.n) : ((key >= past_lo || key < sinkL) && key < L);
             v = vis ? sv : -INFINITY;
             x[nb][2 * hf + e] = v;
           }

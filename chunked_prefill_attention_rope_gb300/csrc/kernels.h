@@ -37,6 +37,7 @@ struct AttnParams {
   const int32_t* n_real;
   const int32_t* sel_row;
   int window, causal;
+  int sink;  // implicit mask: past slots [0, sink) stay visible whatever the window
   uint16_t* out;
   float* out_sel;
   float* part_o;    // split-KV partials [splits][B][Hq][C][D] or null

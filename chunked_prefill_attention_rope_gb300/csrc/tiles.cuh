@@ -14,7 +14,9 @@ constexpr float kEmptyRow = -1e28f;              // running max below this: no v
 // tiles (chunk rows [t*BN, t*BN + BN)), tiles [Tc, Tc + Tp) are past tiles
 // (slots [(t-Tc)*BN, ...)).  Split s owns the fixed index range
 // [s*T/S, (s+1)*T/S) and visits the live tiles inside it.  The implicit mask
-// makes the live set two intervals; with an explicit mask every tile is live.
+// makes the live set two intervals (with sink slots, the past interval starts
+// at slot 0 and the tiles between the sinks and the window are visited,
+// fully masked); with an explicit mask every tile is live.
 // Because the ranges do not depend on the mask, the explicit and implicit
 // descriptions of one mask split the keys identically; the extra tiles the
 // explicit path visits are fully masked and contribute exactly zero.
@@ -44,7 +46,7 @@ __device__ __forceinline__ TilePlan plan_tiles_range(const AttnParams& p, int b,
     const int W = p.window;
     const int t_lo = W > 0 ? max(0, i_min - W + 1) : 0;
     const int t_hi = p.causal ? min(t.n, i_max + 1) : (W > 0 ? min(t.n, i_max + W) : t.n);
-    const int j_lo = W > 0 ? max(0, t.L + i_min - W + 1) : 0;
+    const int j_lo = (W > 0 && p.sink <= 0) ? max(0, t.L + i_min - W + 1) : 0;
     const int j_hi = t.L;
     c0 = t_lo / BN;
     c1 = t_hi > t_lo ? (t_hi + BN - 1) / BN : c0;
@@ -73,20 +75,32 @@ __device__ __forceinline__ TilePlan plan_whole(const AttnParams& p, int b, int i
   return plan_tiles_range<BN>(p, b, i_min, i_max, 0, 1LL << 30);
 }
 
+// Bits [a, b) of a 32-bit word (a and b clipped to [0, 32]).
+__device__ __forceinline__ uint32_t bit_range(int a, int b) {
+  a = min(max(a, 0), 32);
+  b = min(max(b, 0), 32);
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  const uint32_t below_a = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+  return below_b & ~below_a;
+}
+
 // Visible key interval of query row i, relative to a tile's first key
 // (implicit mask): keys e with lo <= e < hi are visible.
 struct RowSpan {
-  int past_lo, ch_lo, ch_hi, L;
+  int past_lo, ch_lo, ch_hi, L, sinkL;
   __device__ __forceinline__ void init(const AttnParams& p, const TilePlan& tp, int i, bool valid) {
     const int W = p.window;
     L = valid ? tp.L : 0;
     past_lo = W > 0 ? max(0, tp.L + i - W + 1) : 0;
     ch_lo = W > 0 ? max(0, i - W + 1) : 0;
     ch_hi = !valid ? 0 : (p.causal ? min(tp.n, i + 1) : (W > 0 ? min(tp.n, i + W) : tp.n));
+    sinkL = min(p.sink, L);
   }
-  __device__ __forceinline__ void tile(bool chunk, int base, int& lo, int& hi) const {
+  // Keys e of the tile with lo <= e < hi, or e < sk (pinned sink slots), are visible.
+  __device__ __forceinline__ void tile(bool chunk, int base, int& lo, int& hi, int& sk) const {
     lo = (chunk ? ch_lo : past_lo) - base;
     hi = (chunk ? ch_hi : L) - base;
+    sk = chunk ? 0 : sinkL - base;
   }
 };
 

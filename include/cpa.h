@@ -108,8 +108,11 @@ typedef struct {
  *            t < n_real[b], (causal == 0 or t <= i) and (window == 0 or
  *            |i - t| < window).  ([P1, Change]: causal band, zero padding,
  *            512-position window; [P2, Mask/cache layout]: packed past,
- *            unfilled slots masked.)  Past slots must map to positions
- *            0..P-1 (a global cache, or a sliding cache without sinks).
+ *            unfilled slots masked.)  A SLIDING cache with sink S > 0 also
+ *            keeps its pinned slots [0, min(S, past_len[b])) visible to
+ *            every row whatever the window; its other slots hold the newest
+ *            tokens in order, so the window rule above applies to them
+ *            ([P4, Fix]: pinned sink rows, chronological compaction).
  *          non-NULL: explicit additive fp32 mask [B, Hq, C, P + C],
  *            contiguous, 0 = attend, -1e30 = masked ([P1, Change]); entries
  *            <= -1e29 count as masked; entries are added to the scaled
@@ -127,7 +130,8 @@ typedef struct {
  *   out_sel  fp32 [B, Hq*D] or NULL: row sel_row[b] of every head, before
  *          bf16 rounding.
  *   workspace  device memory of at least cpa_attn_workspace_size(...) bytes
- *          (split-KV partial results); may be NULL when that size is 0.
+ *          (split-KV partial results, rotated copies of the chunk's queries
+ *          and keys); may be NULL when that size is 0.
  *   err    device int32 error word (required).
  */
 typedef struct {

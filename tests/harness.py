@@ -59,7 +59,7 @@ def cache_bytes(t: torch.Tensor) -> np.ndarray:
 
 
 def oracle_attn(q, k_new, v_new, cos, sin, ck, cv, P, past_len, n_real, window=0, causal=1,
-                mask=None, sel_row=None):
+                mask=None, sel_row=None, sink=0):
     """Run the oracle on host copies of torch tensors."""
     f = lambda t: None if t is None else t.detach().cpu()
     L = f(past_len).numpy() if past_len is not None else None
@@ -68,13 +68,13 @@ def oracle_attn(q, k_new, v_new, cos, sin, ck, cv, P, past_len, n_real, window=0
     s = None if sel_row is None else f(sel_row).numpy()
     return O.chunk_prefill_attn(bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new), f(cos).numpy(),
                                 f(sin).numpy(), bf16_bits(ck), bf16_bits(cv), P, L, n,
-                                window=window, causal=causal, mask=m, sel_row=s)
+                                window=window, causal=causal, mask=m, sel_row=s, sink=sink)
 
 
-def explicit_masks(past_len, n_real, C, P, Hq, window, causal):
+def explicit_masks(past_len, n_real, C, P, Hq, window, causal, sink=0):
     """[B, Hq, C, P+C] fp32 additive masks built by the oracle's mask function."""
     B = len(past_len)
     out = np.zeros((B, Hq, C, P + C), dtype=np.float32)
     for b in range(B):
-        out[b] = O.explicit_mask(int(past_len[b]), int(n_real[b]), C, P, window, causal)[None]
+        out[b] = O.explicit_mask(int(past_len[b]), int(n_real[b]), C, P, window, causal, sink)[None]
     return torch.from_numpy(out)

@@ -70,7 +70,14 @@ def test_host_validation_returns_status_without_launch(lib):
     assert call(_args(cpa, **dict(full, cache=ctypes.pointer(bad)))) == 3  # stride not a multiple of 8
     assert so.cpa_decode_step(ctypes.byref(_args(cpa, **full)), None) == 2  # decode needs C == 1
     sl = cpa._Cache(fake, fake, 64 * 64, 64 * 64, 64, fake, 64, 1, 32, 4)
-    assert call(_args(cpa, **dict(full, cache=ctypes.pointer(sl)))) == 4   # implicit mask with sinks
+    # an implicit mask over a sliding cache with sinks is accepted: validation
+    # stops at the missing workspace, before any launch
+    assert call(_args(cpa, **dict(full, cache=ctypes.pointer(sl)))) == 6
+    # the fused attention + append takes global caches only, and needs n_rows
+    fused = lambda a, n: so.cpa_chunk_prefill_attn_append(ctypes.byref(a), n, None)
+    assert fused(_args(cpa, **dict(full, cache=ctypes.pointer(sl))), fake) == 4
+    assert fused(_args(cpa, **full), None) == 1
+    assert fused(_args(cpa, **full), fake + 4) == 3
 
 
 def test_sliding_guards(lib):

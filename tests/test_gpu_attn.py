@@ -77,6 +77,43 @@ def test_attention_matches_oracle_and_explicit_is_bitwise_implicit(w):
     assert torch.equal(out_2.view(torch.int16), out_i.view(torch.int16)), "not deterministic"
 
 
+SINK_CASES = [
+    # (workload over a full or nearly full sliding window cache of W = P rows, sink rows S)
+    (small("k_pair_d128", 2, 8, 2, 128, 64, 256, ("uniform", 200, 256), ("uniform", 1, 64), window=256), 4),
+    (small("k_single_d256", 1, 8, 1, 256, 128, 512, ("fixed", 512), ("fixed", 127), window=512), 2),
+    (small("k_single_d64", 2, 4, 1, 64, 16, 96, ("uniform", 80, 96), ("uniform", 1, 16), window=96), 3),
+    (small("k_decode", 4, 8, 2, 128, 1, 512, ("uniform", 400, 512), ("fixed", 1), window=300, causal=0), 4),
+    (small("k_decode_g32", 1, 32, 1, 128, 1, 300, ("fixed", 300), ("fixed", 1), window=200, causal=0), 5),
+]
+
+
+@pytest.mark.parametrize("w,S", SINK_CASES, ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_sink_aware_implicit_mask(w, S):
+    """A sliding cache with S pinned sink rows and the implicit mask: the sink
+    slots stay visible whatever the window (the oracle's reading of the pinned
+    rows in "Pad the chunked-prefill tail for sliding-window models"); the
+    explicit mask built from the same rule gives the same bits."""
+    cpa = lib()
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    out_i, sel_i, err = run_gpu(cpa, inp, ck, cv, w.P, w.window, bool(w.causal), kind=cpa.SLIDING, wsize=w.P,
+                                sink=S)
+    assert int(err[0]) == 0
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                               inp["past_len"], inp["n_real"], w.window, w.causal,
+                               sel_row=(inp["n_real"] - 1).clamp(min=0), sink=S)
+    assert_close(out_i, ref, w.name)
+    check_argmax(sel_i, ref_sel, w.name)
+    # the sinks matter here: without them the oracle's answer differs
+    ref0, _ = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                          inp["past_len"], inp["n_real"], w.window, w.causal, sink=0)
+    assert np.abs(ref0 - ref).max() > 1e-3
+    mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, w.window, w.causal, S)
+    out_e, _, err = run_gpu(cpa, inp, ck, cv, w.P, mask=mask, kind=cpa.SLIDING, wsize=w.P, sink=S)
+    assert int(err[0]) == 0
+    assert torch.equal(out_e.view(torch.int16), out_i.view(torch.int16)), "explicit != implicit"
+
+
 def test_implicit_ignores_dead_cache_rows():
     """Slots at or past past_len never influence the implicit path."""
     cpa = lib()
