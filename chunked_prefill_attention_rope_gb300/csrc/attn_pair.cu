@@ -278,7 +278,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) 
   }
 }
 
-template <int D, bool EXPLICIT>
+// SINK: the implicit mask also keeps pinned sink slots visible (a separate
+// instantiation, so the common case carries none of that code).
+template <int D, bool EXPLICIT, bool SINK>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                      const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 #pragma unroll
           for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
           if (__any_sync(0xffffffffu, lo > 0 || hi < kBN)) {
-            if (!__any_sync(0xffffffffu, sk > 0)) {
+            if (!SINK || !__any_sync(0xffffffffu, sk > 0)) {
 #pragma unroll
               for (int q = 0; q < kBN; ++q) sc[q] = (q >= lo && q < hi) ? sc[q] : -INFINITY;
             } else {
@@ -861,10 +863,10 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
   return w;
 }
 
-template <int D, bool EXPLICIT>
+template <int D, bool EXPLICIT, bool SINK = false>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   constexpr int smem = pair_smem_bytes<D>();
-  auto kern = attn_pair_kernel<D, EXPLICIT>;
+  auto kern = attn_pair_kernel<D, EXPLICIT, SINK>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -888,8 +890,13 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   const bool ex = p.mask != nullptr;
   switch (p.D) {
-    case 64: return ex ? launch_pair_t<64, true>(maps, p, stream) : launch_pair_t<64, false>(maps, p, stream);
-    case 128: return ex ? launch_pair_t<128, true>(maps, p, stream) : launch_pair_t<128, false>(maps, p, stream);
+    case 64:
+      return ex ? launch_pair_t<64, true>(maps, p, stream)
+                : (p.sink > 0 ? launch_pair_t<64, false, true>(maps, p, stream) : launch_pair_t<64, false>(maps, p, stream));
+    case 128:
+      return ex ? launch_pair_t<128, true>(maps, p, stream)
+                : (p.sink > 0 ? launch_pair_t<128, false, true>(maps, p, stream)
+                              : launch_pair_t<128, false>(maps, p, stream));
     default: return cudaErrorInvalidValue;
   }
 }
