@@ -48,9 +48,9 @@ KERNEL_SOURCES = {
 }
 MEASURED_TRAFFIC = {
     # long-context chunk call: prep + attn_pair + merge, one ncu capture of the second call
-    "prefill": {"src": "2f9cb6bc36a8d83e", "bytes": 657344768},
+    "prefill": {"src": "f56f192a66450fea", "bytes": 656865280},
     # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0084 x)
-    "decode": {"src": "7b429be1ffa154a5", "bytes": 4836439267},
+    "decode": {"src": "6585a081aaf39936", "bytes": 4836503778},
 }
 
 def source_hash(kind):
