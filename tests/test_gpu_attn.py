@@ -52,6 +52,13 @@ CASES = [
     small("d_decode_win", 2, 8, 2, 64, 1, 900, ("uniform", 300, 900), ("fixed", 1), window=100, causal=0),
     small("d_decode_g16", 2, 16, 1, 128, 1, 257, ("uniform", 0, 257), ("fixed", 1), causal=0),
     small("d_decode_g32", 1, 32, 1, 128, 1, 300, ("fixed", 299), ("fixed", 1), causal=0),
+    # edge shapes: one chunk row per packed tile row (G = 128), a long prefill
+    # without past, D = 256 without grouping, a ragged C of 1 row past a tile
+    small("e_g128", 1, 128, 1, 64, 8, 100, ("fixed", 100), ("fixed", 7)),
+    small("e_prefill_1024", 1, 8, 8, 128, 1024, 0, ("fixed", 0), ("fixed", 1000)),
+    small("e_d256_g1", 2, 2, 2, 256, 200, 130, ("uniform", 0, 130), ("uniform", 1, 200)),
+    small("e_ragged_129", 2, 4, 2, 128, 129, 257, ("uniform", 0, 257), ("fixed", 129)),
+    small("e_all_pad", 2, 8, 2, 128, 64, 64, ("fixed", 0), ("fixed", 0)),
 ]
 
 
