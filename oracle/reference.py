@@ -23,6 +23,13 @@ the design notes):
 
 bf16 tensors are passed as numpy uint16 arrays of raw bit patterns.
 
+A cache may hold fp16 instead of bf16 (kv="f16"; the padded-tail page
+mentions a runtime option that stores the KV cache in fp16).  Reading taken:
+the rotation arithmetic is unchanged and only its final rounding is to fp16;
+V rows are converted bf16 -> fp16 to nearest-even; the attention then sees Q
+and the chunk keys rotated to fp16 as well (one precision for all products),
+and values in fp16.  fp16 cache arrays are uint16 bit patterns too.
+
 Parity: every function here is pinned by tests/test_oracle_pins.py and
 tests/test_oracle_invariants.py (closed forms, invariants, a library routine
 on the special cases that reduce to textbook attention, brute force).
@@ -35,10 +42,10 @@ MASKED = -1e30          # the additive value the pages give for "masked" [P1, Ch
 MASK_LIMIT = -1e29      # an entry at or below this counts as masked
 
 __all__ = [
-    "MASKED", "MASK_LIMIT", "bf16_to_f32", "f32_to_bf16", "rope_rotate",
+    "MASKED", "MASK_LIMIT", "bf16_to_f32", "f32_to_bf16", "f16_to_f32", "f32_to_f16", "rope_rotate",
     "visible", "explicit_mask", "attend", "chunk_prefill_attn", "decode_step",
     "kv_append_global", "kv_append_sliding", "snapshot_padded_append",
-    "rollback_padded_append", "select_argmax",
+    "rollback_padded_append", "select_argmax", "kv_to_f32", "to_kv",
 ]
 
 
@@ -58,10 +65,33 @@ def f32_to_bf16(x) -> np.ndarray:
     return r.astype(np.uint16)
 
 
+def f16_to_f32(bits) -> np.ndarray:
+    """IEEE half bit patterns -> float32 (exact widening)."""
+    return np.ascontiguousarray(np.asarray(bits, dtype=np.uint16)).view(np.float16).astype(np.float32)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """float32 -> IEEE half bit patterns, round to nearest, ties to even
+    (numpy's IEEE conversion; beyond the half range it gives +-inf)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def kv_to_f32(bits, kv: str = "bf16") -> np.ndarray:
+    """Cache-format bit patterns (bf16 or f16) -> float32."""
+    return bf16_to_f32(bits) if kv == "bf16" else f16_to_f32(bits)
+
+
+def to_kv(bf16_bits, kv: str = "bf16") -> np.ndarray:
+    """bf16 bit patterns in the cache format (f16: nearest-even conversion)."""
+    return np.asarray(bf16_bits, dtype=np.uint16) if kv == "bf16" else f32_to_f16(bf16_to_f32(bf16_bits))
+
+
 # ---------------------------------------------------------------- RoPE
 
-def rope_rotate(x_bits, cos, sin) -> np.ndarray:
-    """Rotate bf16 rows with per-row cos/sin tables; returns bf16 bits.
+def rope_rotate(x_bits, cos, sin, out: str = "bf16") -> np.ndarray:
+    """Rotate bf16 rows with per-row cos/sin tables; returns bf16 bits (or f16
+    bits with out="f16": the same fp32 values, rounded to half).
 
     [P1, Change]: RoPE from per-position [C, headDim] cos/sin tables.
     [P2, Runtime behavior]: position_embeddings = (cos_t, sin_t).
@@ -78,7 +108,8 @@ def rope_rotate(x_bits, cos, sin) -> np.ndarray:
     lo, hi = x[..., :h], x[..., h:]
     y_lo = np.subtract(np.multiply(lo, c[..., :h]), np.multiply(hi, s[..., :h]))
     y_hi = np.add(np.multiply(hi, c[..., h:]), np.multiply(lo, s[..., h:]))
-    return f32_to_bf16(np.concatenate([y_lo, y_hi], axis=-1))
+    y = np.concatenate([y_lo, y_hi], axis=-1)
+    return f32_to_bf16(y) if out == "bf16" else f32_to_f16(y)
 
 
 # ---------------------------------------------------------------- masks
@@ -148,7 +179,7 @@ def attend(q, keys, values, add_mask, scale: float) -> np.ndarray:
 
 
 def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, n_real,
-                       window=0, causal=1, mask=None, scale=None, sel_row=None, sink=0):
+                       window=0, causal=1, mask=None, scale=None, sel_row=None, sink=0, kv="bf16"):
     """One chunk of C rows attending over P cached slots plus the chunk itself.
 
     [P1, Change]: heads-first [heads, C, headDim] Q/K/V, RoPE from the cos/sin
@@ -156,7 +187,8 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
     [1, nHeads, C, past+C], K/V extended by the chunk, one-hot select of a row.
     GQA: q head h reads kv head h // (Hq // Hkv).
 
-    q [B,Hq,C,D], k_new/v_new [B,Hkv,C,D], cache_k/cache_v [B,Hkv,>=P,D]: bf16 bits.
+    q [B,Hq,C,D], k_new/v_new [B,Hkv,C,D]: bf16 bits; cache_k/cache_v
+    [B,Hkv,>=P,D]: bits in the cache format kv ("bf16" or "f16").
     cos/sin [B,C,D] fp32.  mask: None (implicit from past_len, n_real, window,
     causal, sink) or fp32 [B,Hq,C,P+C].  Returns (out fp64 [B,Hq,C,D],
     out_sel fp64 [B,Hq*D] or None).
@@ -168,18 +200,18 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
     sc = (1.0 / np.sqrt(D)) if scale is None or scale <= 0 else float(scale)
     cos = np.asarray(cos, dtype=np.float32)
     sin = np.asarray(sin, dtype=np.float32)
-    q_rot = bf16_to_f32(rope_rotate(q, cos[:, None], sin[:, None])).astype(np.float64)
-    k_rot = bf16_to_f32(rope_rotate(k_new, cos[:, None], sin[:, None])).astype(np.float64)
-    v_chk = bf16_to_f32(v_new).astype(np.float64)
+    q_rot = kv_to_f32(rope_rotate(q, cos[:, None], sin[:, None], kv), kv).astype(np.float64)
+    k_rot = kv_to_f32(rope_rotate(k_new, cos[:, None], sin[:, None], kv), kv).astype(np.float64)
+    v_chk = kv_to_f32(to_kv(v_new, kv), kv).astype(np.float64)
     out = np.zeros((B, Hq, C, D), dtype=np.float64)
     for b in range(B):
         L, n = int(past_len[b]), int(n_real[b])
         implicit = None if mask is not None else explicit_mask(L, n, C, P, window, causal, sink)
         for h in range(Hq):
             kvh = h // G
-            keys = np.concatenate([bf16_to_f32(cache_k[b, kvh, :P]).astype(np.float64),
+            keys = np.concatenate([kv_to_f32(cache_k[b, kvh, :P], kv).astype(np.float64),
                                    k_rot[b, kvh]], axis=0)
-            vals = np.concatenate([bf16_to_f32(cache_v[b, kvh, :P]).astype(np.float64),
+            vals = np.concatenate([kv_to_f32(cache_v[b, kvh, :P], kv).astype(np.float64),
                                    v_chk[b, kvh]], axis=0)
             add = implicit if mask is None else np.asarray(mask[b, h], dtype=np.float32)
             out[b, h] = attend(q_rot[b, h], keys, vals, add, sc)
@@ -189,7 +221,7 @@ def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len,
     return out, out_sel
 
 
-def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window=0, sink=0):
+def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window=0, sink=0, kv="bf16"):
     """One-token decode: the C = 1 case.
 
     [P2, Mask/cache layout]: the mask unmasks the valid past slots and the
@@ -198,7 +230,7 @@ def decode_step(q, k_new, v_new, cos, sin, cache_k, cache_v, P, past_len, window
     B = np.asarray(q).shape[0]
     ones = np.ones(B, dtype=np.int64)
     out, _ = chunk_prefill_attn(q, k_new, v_new, cos, sin, cache_k, cache_v, P,
-                                past_len, ones, window=window, causal=0, sink=sink)
+                                past_len, ones, window=window, causal=0, sink=sink, kv=kv)
     return out
 
 
@@ -209,7 +241,7 @@ def select_argmax(out_sel_f32) -> np.ndarray:
 
 # ---------------------------------------------------------------- caches
 
-def kv_append_global(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows):
+def kv_append_global(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows, kv="bf16"):
     """Append the rotated chunk K and the chunk V after the cached rows (in place).
 
     [P2, Runtime behavior]: the runtime writes each step's KV into external
@@ -217,9 +249,11 @@ def kv_append_global(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows):
     [0, n_b) of the chunk go to slots [len_b, len_b + n_b) and len_b grows by
     n_b.  A sequence whose rows do not fit (len_b + n_b > capacity) is left
     unchanged and reported.  Returns the list of overflowing sequences.
+    kv: the cache format ("bf16" or "f16").
     """
     cap = cache_k.shape[2]
-    k_rot = rope_rotate(k_new, np.asarray(cos)[:, None], np.asarray(sin)[:, None])
+    k_rot = rope_rotate(k_new, np.asarray(cos)[:, None], np.asarray(sin)[:, None], kv)
+    v_kv = to_kv(v_new, kv)
     overflow = []
     for b in range(cache_k.shape[0]):
         L, n = int(length[b]), int(n_rows[b])
@@ -227,13 +261,13 @@ def kv_append_global(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows):
             overflow.append(b)
             continue
         cache_k[b, :, L:L + n] = k_rot[b, :, :n]
-        cache_v[b, :, L:L + n] = np.asarray(v_new)[b, :, :n]
+        cache_v[b, :, L:L + n] = v_kv[b, :, :n]
         length[b] = L + n
     return overflow
 
 
 def kv_append_sliding(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows,
-                      window: int, sink: int = 0):
+                      window: int, sink: int = 0, kv="bf16"):
     """Append to a sliding-window cache that compacts chronologically (in place).
 
     [P4, Fix]: sliding caches compact chronologically on eviction; the oldest
@@ -244,7 +278,8 @@ def kv_append_sliding(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows,
     sequences breaking that are left unchanged and returned.
     """
     W, S = int(window), int(sink)
-    k_rot = rope_rotate(k_new, np.asarray(cos)[:, None], np.asarray(sin)[:, None])
+    k_rot = rope_rotate(k_new, np.asarray(cos)[:, None], np.asarray(sin)[:, None], kv)
+    v_kv = to_kv(v_new, kv)
     bad = []
     for b in range(cache_k.shape[0]):
         L, n = int(length[b]), int(n_rows[b])
@@ -252,7 +287,7 @@ def kv_append_sliding(cache_k, cache_v, length, k_new, v_new, cos, sin, n_rows,
             bad.append(b)
             continue
         e = max(0, L + n - W)
-        for cache, new in ((cache_k, k_rot), (cache_v, np.asarray(v_new))):
+        for cache, new in ((cache_k, k_rot), (cache_v, v_kv)):
             rows = np.concatenate([cache[b, :, :min(S, L)], cache[b, :, S + e:L], new[b, :, :n]],
                                   axis=1)
             cache[b, :, :rows.shape[1]] = rows

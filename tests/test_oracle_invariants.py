@@ -40,7 +40,7 @@ def tables(pos0, C, D, base=10000.0):
     return c.numpy(), s.numpy()
 
 
-def run_chunked_global(q, k, v, sizes, C, window=0):
+def run_chunked_global(q, k, v, sizes, C, window=0, kv="bf16"):
     _, Hq, T, D = q.shape
     Hkv = k.shape[1]
     cap = T + C
@@ -53,21 +53,22 @@ def run_chunked_global(q, k, v, sizes, C, window=0):
         cos, sin = tables(L, C, D)
         qc, kc, vc = chunk_of(q, s, s + n, C), chunk_of(k, s, s + n, C), chunk_of(v, s, s + n, C)
         out, _ = O.chunk_prefill_attn(qc, kc, vc, cos, sin, ck, cv, L, [L], [n],
-                                      window=window, causal=1)
+                                      window=window, causal=1, kv=kv)
         outs.append(out[:, :, :n])
-        assert O.kv_append_global(ck, cv, length, kc, vc, cos, sin, [n]) == []
+        assert O.kv_append_global(ck, cv, length, kc, vc, cos, sin, [n], kv=kv) == []
         s += n
     assert s == T
     return np.concatenate(outs, axis=2), ck, cv, length
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,window", [(16, 4, 1, 0), (32, 4, 2, 0), (16, 2, 2, 5)])
-def test_invariant_a_chunks_equal_full_pass_equal_decode(D, Hq, Hkv, window):
+@pytest.mark.parametrize("D,Hq,Hkv,window,kv", [(16, 4, 1, 0, "bf16"), (32, 4, 2, 0, "bf16"), (16, 2, 2, 5, "bf16"),
+                                                (16, 4, 1, 0, "f16"), (32, 4, 2, 5, "f16")])
+def test_invariant_a_chunks_equal_full_pass_equal_decode(D, Hq, Hkv, window, kv):
     T = 23
     q, k, v = stream(T, Hq, Hkv, D, f"inv_a/{D}/{Hkv}/{window}")
-    full, fk, fv, fl = run_chunked_global(q, k, v, [T], T, window)
+    full, fk, fv, fl = run_chunked_global(q, k, v, [T], T, window, kv)
     for sizes, C in (([8, 8, 7], 8), ([5, 5, 5, 5, 3], 8), ([16, 7], 16), ([3, 11, 9], 12)):
-        out, ck, cv, cl = run_chunked_global(q, k, v, sizes, C, window)
+        out, ck, cv, cl = run_chunked_global(q, k, v, sizes, C, window, kv)
         assert np.max(np.abs(out - full)) < 1e-12
         assert cl[0] == fl[0] == T
         assert np.array_equal(ck[:, :, :T], fk[:, :, :T]) and np.array_equal(cv[:, :, :T], fv[:, :, :T])
@@ -80,9 +81,9 @@ def test_invariant_a_chunks_equal_full_pass_equal_decode(D, Hq, Hkv, window):
     for t in range(T):
         cos, sin = tables(t, 1, D)
         out = O.decode_step(q[:, :, t:t + 1], k[:, :, t:t + 1], v[:, :, t:t + 1], cos, sin,
-                            dk, dv, t, [t], window=window)
+                            dk, dv, t, [t], window=window, kv=kv)
         outs.append(out)
-        O.kv_append_global(dk, dv, length, k[:, :, t:t + 1], v[:, :, t:t + 1], cos, sin, [1])
+        O.kv_append_global(dk, dv, length, k[:, :, t:t + 1], v[:, :, t:t + 1], cos, sin, [1], kv=kv)
     dec = np.concatenate(outs, axis=2)
     assert np.max(np.abs(dec - full)) < 1e-12
     assert np.array_equal(dk[:, :, :T], fk[:, :, :T]) and np.array_equal(dv[:, :, :T], fv[:, :, :T])
@@ -238,3 +239,30 @@ def test_invariant_c_explicit_equals_implicit(window, causal):
                                       sel_row=[4, 7])
     assert np.array_equal(imp, exp) and np.array_equal(sel_i, sel_e)
     assert np.array_equal(sel_i[1].reshape(Hq, D), imp[1, :, 7])
+
+
+def test_f16_cache_holds_rotated_keys_rounded_to_half():
+    """The f16 cache's key rows are the bf16 path's fp32 rotation rounded to half
+    (closed form against the rotation done with exact fp64 products, within one
+    fp32 rounding), values are the bf16 rows converted exactly; and attention over
+    the f16 cache differs from the bf16 one only by rounding."""
+    D, Hkv, C = 32, 2, 6
+    k = bf16_bits(normal_bf16((1, Hkv, C, D), 0, "f16c/k"))
+    v = bf16_bits(normal_bf16((1, Hkv, C, D), 0, "f16c/v"))
+    cos, sin = tables(100, C, D)
+    ck = np.zeros((1, Hkv, C, D), np.uint16); cv = ck.copy(); ln = np.zeros(1, np.int64)
+    O.kv_append_global(ck, cv, ln, k, v, cos, sin, [C], kv="f16")
+    x = O.bf16_to_f32(k).astype(np.float64)
+    h = D // 2
+    c64, s64 = cos.astype(np.float64)[None, None], sin.astype(np.float64)[None, None]
+    exact = np.concatenate([x[..., :h] * c64[..., :h] - x[..., h:] * s64[..., :h],
+                            x[..., h:] * c64[..., h:] + x[..., :h] * s64[..., h:]], axis=-1)
+    got = O.f16_to_f32(ck).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= np.abs(exact) * 2.0 ** -11 + 2.0 ** -24 + 4 * 2.0 ** -24 * np.abs(x).max())
+    assert np.array_equal(O.f16_to_f32(cv), O.bf16_to_f32(v))
+    q, kk, vv = stream(9, 4, 2, 32, "f16c/attn")
+    cos2, sin2 = tables(0, 9, 32)
+    e = np.zeros((1, 2, 0, 32), np.uint16)
+    a16, _ = O.chunk_prefill_attn(q, kk, vv, cos2, sin2, e, e, 0, [0], [9], kv="f16")
+    a32, _ = O.chunk_prefill_attn(q, kk, vv, cos2, sin2, e, e, 0, [0], [9], kv="bf16")
+    assert 0 < np.abs(a16 - a32).max() < 2e-2

@@ -49,6 +49,35 @@ def test_bf16_round_trip_and_rne_matches_torch():
     assert np.array_equal(O.f32_to_bf16(O.bf16_to_f32(ours)), ours)
 
 
+def test_f16_conversions_match_torch():
+    """fp32 -> fp16 nearest-even (ties, subnormals, overflow) and fp16 -> fp32
+    widening of every bit pattern, against torch's conversions."""
+    rng = np.random.default_rng(2)
+    x = np.concatenate([rng.standard_normal(100000).astype(np.float32) * np.float32(3e3),
+                        rng.standard_normal(10000).astype(np.float32) * np.float32(1e-5),
+                        np.float32([0.0, -0.0, 65504.0, 65520.0, 7e4, -7e4, 6.1e-5, 5.96e-8, 1e-9])])
+    base = O.f16_to_f32(O.f32_to_f16(x[:1000]))
+    ulp = np.abs(np.spacing(base.astype(np.float16)).astype(np.float32))
+    ties = base + ulp * np.float32(0.5)          # exactly halfway between two halves
+    x = np.concatenate([x, ties])
+    ours = O.f32_to_f16(x)
+    lib = torch.from_numpy(x).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, lib)
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    wide = O.f16_to_f32(bits)
+    lib_w = torch.from_numpy(bits.view(np.int16)).view(torch.float16).float().numpy()
+    same = (wide.view(np.uint32) == lib_w.view(np.uint32)) | (np.isnan(wide) & np.isnan(lib_w))
+    assert same.all()
+
+
+def test_cache_format_helpers():
+    """bf16 -> f16 conversion is exact inside the half range; bf16 stays as is."""
+    v = bf16_bits(normal_bf16((4, 64), 0, "pin/to_kv"))
+    assert np.array_equal(O.to_kv(v, "bf16"), v)
+    h = O.to_kv(v, "f16")
+    assert np.array_equal(O.kv_to_f32(h, "f16"), O.bf16_to_f32(v))   # N(0,1) values fit fp16 exactly
+
+
 # ------------------------------------------------------------------ RoPE
 
 def test_rope_hand_worked_example():
@@ -65,15 +94,17 @@ def test_rope_position_zero_is_identity():
     cos, sin = rope_tables(np.zeros((5,)), 64, 10000.0)
     assert np.all(cos.numpy() == 1.0) and np.all(sin.numpy() == 0.0)
     assert np.array_equal(O.rope_rotate(x, cos.numpy(), sin.numpy()), x)
+    # in the half format the same rows, converted exactly
+    assert np.array_equal(O.f16_to_f32(O.rope_rotate(x, cos.numpy(), sin.numpy(), "f16")), O.bf16_to_f32(x))
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
-def test_rope_matches_complex_rotation(D):
+@pytest.mark.parametrize("D,out", [(64, "bf16"), (128, "bf16"), (256, "bf16"), (128, "f16"), (256, "f16")])
+def test_rope_matches_complex_rotation(D, out):
     """Pair (x_d, x_{d+D/2}) as z = x_d + i x_{d+D/2}; RoPE multiplies z by cos + i sin."""
     x = bf16_bits(normal_bf16((7, D), 0, f"pin/rope_c{D}"))
     pos = np.arange(7) * 131 + 5
     cos, sin = [t.numpy() for t in rope_tables(pos, D, 10000.0)]
-    y = f64(O.rope_rotate(x, cos, sin))
+    y = O.kv_to_f32(O.rope_rotate(x, cos, sin, out), out).astype(np.float64)
     h = D // 2
     xf = f64(x)
     z = (xf[:, :h] + 1j * xf[:, h:]) * (cos[:, :h].astype(np.float64) + 1j * sin[:, :h].astype(np.float64))
@@ -82,7 +113,8 @@ def test_rope_matches_complex_rotation(D):
     # then one bf16 rounding (<= half a bf16 ulp of the larger of the two values)
     pair = np.concatenate([np.abs(xf[:, :h]) + np.abs(xf[:, h:])] * 2, axis=1)
     top = np.maximum(np.abs(exact), np.abs(y))
-    ulp = np.exp2(np.floor(np.log2(np.maximum(top, 1e-30))) - 7)
+    mant = 7 if out == "bf16" else 10   # stored mantissa bits of the output format
+    ulp = np.exp2(np.floor(np.log2(np.maximum(top, 2.0 ** -14))) - mant)
     assert np.all(np.abs(y - exact) <= 0.5 * ulp + 3 * 2.0 ** -24 * pair)
     # and the tolerance is tight enough that a wrong sign or pairing would fail
     wrong = np.concatenate([z.real, -z.imag], axis=1)
