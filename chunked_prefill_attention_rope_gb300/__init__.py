@@ -50,7 +50,7 @@ class _Cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
                 ("stride_h", ctypes.c_int64), ("stride_s", ctypes.c_int64), ("len", ctypes.c_void_p),
                 ("cap", ctypes.c_int32), ("kind", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("sink", ctypes.c_int32)]
+                ("sink", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 class _AttnArgs(ctypes.Structure):
@@ -135,13 +135,13 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None):
 
 
 class KVCache:
-    """One layer's KV cache: k, v bf16 [B, Hkv, cap, D] (strided views allowed,
-    last dim contiguous), len int32 [B] on the device, and its kind."""
+    """One layer's KV cache: k, v bf16 or fp16 [B, Hkv, cap, D] (strided views
+    allowed, last dim contiguous), len int32 [B] on the device, and its kind."""
 
     def __init__(self, k: torch.Tensor, v: torch.Tensor, length: torch.Tensor, kind: int = GLOBAL,
                  window: int = 0, sink: int = 0):
-        if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-            raise TypeError("cache k/v must be bf16")
+        if k.dtype not in (torch.bfloat16, torch.float16) or v.dtype != k.dtype:
+            raise TypeError("cache k/v must both be bf16 or both fp16")
         if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 4 or k.stride(3) != 1:
             raise ValueError("cache k/v: same [B, Hkv, cap, D] shape and strides, last dim contiguous")
         _need(length, "len", torch.int32, (k.shape[0],))
@@ -151,7 +151,8 @@ class KVCache:
 
     def struct(self) -> _Cache:
         return _Cache(self.k.data_ptr(), self.v.data_ptr(), self.k.stride(0), self.k.stride(1),
-                      self.k.stride(2), self.len.data_ptr(), self.cap, self.kind, self.window, self.sink)
+                      self.k.stride(2), self.len.data_ptr(), self.cap, self.kind, self.window, self.sink,
+                      1 if self.k.dtype == torch.float16 else 0)
 
 
 def attn_workspace_size(B, Hq, Hkv, D, C, P) -> int:

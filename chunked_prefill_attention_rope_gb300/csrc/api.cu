@@ -99,7 +99,7 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
 // Workspace of the decode and single-tile paths: split-KV partials (when
 // combine_kernel merges them), then the rotated chunk keys (single-tile path).
 struct SingleWorkspace {
-  size_t part_o, part_lse, k_rot, total;
+  size_t part_o, part_lse, k_rot, v_cvt, total;
 };
 SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -114,6 +114,8 @@ SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int 
   }
   if (g.path == kPathSingle) {
     w.k_rot = off;
+    off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
+    w.v_cvt = off;  // fp16 cache: the chunk values in half
     off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
   }
   w.total = off;
@@ -133,6 +135,7 @@ cpa_status check_cache(const cpa_cache* c, int D) {
   if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->len)) return CPA_ERR_ALIGN;
   if (c->stride_s % 8 || c->stride_h % 8 || c->stride_b % 8) return CPA_ERR_ALIGN;
   if (c->kind != CPA_CACHE_GLOBAL && c->kind != CPA_CACHE_SLIDING) return CPA_ERR_SHAPE;
+  if (c->dtype != CPA_KV_BF16 && c->dtype != CPA_KV_F16) return CPA_ERR_UNSUPPORTED;
   if (c->kind == CPA_CACHE_SLIDING) {
     if (c->window < 1 || c->window > c->cap || c->sink < 0 || c->sink >= c->window) return CPA_ERR_SHAPE;
   }
@@ -150,6 +153,7 @@ CacheView view_of(const cpa_cache* c) {
   v.cap = c->cap;
   v.window = c->kind == CPA_CACHE_SLIDING ? c->window : c->cap;
   v.sink = c->kind == CPA_CACHE_SLIDING ? c->sink : 0;
+  v.f16 = c->dtype == CPA_KV_F16 ? 1 : 0;
   return v;
 }
 
@@ -210,6 +214,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.sel_row = a->sel_row;
   p.window = a->window;
   p.causal = a->causal ? 1 : 0;
+  p.f16 = c->dtype == CPA_KV_F16 ? 1 : 0;
   p.sink = (!a->mask && a->cache->kind == CPA_CACHE_SLIDING) ? a->cache->sink : 0;
   p.out = static_cast<uint16_t*>(a->out);
   p.out_sel = a->out_sel;
@@ -243,10 +248,13 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     p.ptag = reinterpret_cast<int32_t*>(w + L.ptag);
     p.q_rot = reinterpret_cast<uint16_t*>(w + L.q_rot);
     p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
+    p.v_cvt = reinterpret_cast<uint16_t*>(w + L.v_cvt);
     // chunk keys and queries come from the rotated copies the pre-pass writes
+    // (and, for an fp16 cache, the chunk values from its half copy)
     CUtensorMap pm[5] = {maps[0], maps[1], maps[2], maps[3], maps[4]};
     if (!make_map(&pm[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn) ||
-        !make_map(&pm[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G))
+        !make_map(&pm[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G) ||
+        (p.f16 && !make_map(&pm[3], p.v_cvt, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn)))
       return CPA_ERR_CUDA;
     return launch_attn_pair5(pm, p, stream) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
   }
@@ -259,8 +267,10 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   if (g.path == kPathSingle) {
     // raw Q rows (box {64, R, G, 1}); chunk keys from the rotated copy
     p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
+    p.v_cvt = reinterpret_cast<uint16_t*>(w + L.v_cvt);
     if (!make_map(&maps[4], a->q, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G) ||
-        !make_map(&maps[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn))
+        !make_map(&maps[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn) ||
+        (p.f16 && !make_map(&maps[3], p.v_cvt, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn)))
       return CPA_ERR_CUDA;
   }
   if (launch_attn(maps, p, stream) != cudaSuccess) return CPA_ERR_CUDA;

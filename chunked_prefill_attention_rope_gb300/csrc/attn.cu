@@ -90,7 +90,7 @@ struct AttnSmem {
   static_assert(kAlloc <= 232448, "shared memory");
 };
 
-template <int D, int BN>
+template <int D, int BN, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                 const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
@@ -219,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(kBM, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, true);
+      constexpr uint32_t idesc_qk = idesc_16(kBM, BN, false, F16);
+      constexpr uint32_t idesc_pv = idesc_16(kBM, D, true, F16);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t p_addr = smem_u32(sP);
       bool ok = my_nt > 0 ? mbar_wait(&bars->q_ready, 0, abort) : true;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* pl = reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8));
             uint4* ph = reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8));
             uint4 lo = *pl, hi = *ph;
-            rope_apply(lo, hi, qtab[u]);
+            rope_apply<F16>(lo, hi, qtab[u]);
             *pl = lo;
             *ph = hi;
           }
@@ -445,10 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c8 = 0; c8 < BN / 8; ++c8) {
         uint4 w;
-        w.x = pack_bf16x2(x[8 * c8 + 0], x[8 * c8 + 1]);
-        w.y = pack_bf16x2(x[8 * c8 + 2], x[8 * c8 + 3]);
-        w.z = pack_bf16x2(x[8 * c8 + 4], x[8 * c8 + 5]);
-        w.w = pack_bf16x2(x[8 * c8 + 6], x[8 * c8 + 7]);
+        w.x = pack16x2<F16>(x[8 * c8 + 0], x[8 * c8 + 1]);
+        w.y = pack16x2<F16>(x[8 * c8 + 2], x[8 * c8 + 3]);
+        w.z = pack16x2<F16>(x[8 * c8 + 4], x[8 * c8 + 5]);
+        w.w = pack16x2<F16>(x[8 * c8 + 6], x[8 * c8 + 7]);
         *reinterpret_cast<uint4*>(sP + (c8 / 8) * (kBM * 128) + sw128(row, c8 % 8)) = w;
       }
       fence_async_smem();
@@ -656,7 +656,17 @@ __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
     uint4 hi = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
     const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
     const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
-    rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    if (p.f16) {
+      rope_pair<true>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+      // the chunk's values in half, for the P V products
+      const uint16_t* vs = p.v_new + r * D;
+      uint16_t* vd = p.v_cvt + r * D;
+      *reinterpret_cast<uint4*>(vd + kc * 8) = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(vs + kc * 8)));
+      *reinterpret_cast<uint4*>(vd + D / 2 + kc * 8) =
+          bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(vs + D / 2 + kc * 8)));
+    } else {
+      rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    }
     uint16_t* dst = p.k_rot + r * D;
     *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
     *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
@@ -722,10 +732,10 @@ __global__ void combine_kernel(const AttnParams p) {
 
 // ------------------------------------------------------------------ host side
 
-template <int D, int BN>
+template <int D, int BN, bool F16>
 static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   using SM = AttnSmem<D, BN>;
-  auto kern = attn_kernel<D, BN>;
+  auto kern = attn_kernel<D, BN, F16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
@@ -759,11 +769,12 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
-// Whether clusters of `splits` CTAs of attn_kernel<D, BN> fit on the device.
+// Whether clusters of `splits` CTAs of attn_kernel<D, BN> fit on the device
+// (the fp16 instantiation has the same resources).
 template <int D, int BN>
 static bool cluster_fits(int splits) {
   using SM = AttnSmem<D, BN>;
-  auto kern = attn_kernel<D, BN>;
+  auto kern = attn_kernel<D, BN, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc) != cudaSuccess) {
     cudaGetLastError();
     return false;
@@ -831,9 +842,15 @@ cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream
     e = launch_attn_decode(maps, p, stream);
   } else {
     switch (p.D) {
-      case 64: e = launch_attn_t<64, 128>(maps, p, stream); break;
-      case 128: e = launch_attn_t<128, 128>(maps, p, stream); break;
-      case 256: e = launch_attn_t<256, 64>(maps, p, stream); break;
+      case 64:
+        e = p.f16 ? launch_attn_t<64, 128, true>(maps, p, stream) : launch_attn_t<64, 128, false>(maps, p, stream);
+        break;
+      case 128:
+        e = p.f16 ? launch_attn_t<128, 128, true>(maps, p, stream) : launch_attn_t<128, 128, false>(maps, p, stream);
+        break;
+      case 256:
+        e = p.f16 ? launch_attn_t<256, 64, true>(maps, p, stream) : launch_attn_t<256, 64, false>(maps, p, stream);
+        break;
       default: return cudaErrorInvalidValue;
     }
   }

@@ -269,7 +269,18 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) 
     for (int u = 0; u < kPrepHeads; ++u) {
       const int hh = grp * kPrepHeads + u;
       if (hh >= HH) break;
-      rope_apply(lo[u], hi[u], tab);
+      if (p.f16) {
+        rope_apply<true>(lo[u], hi[u], tab);
+        if (hh >= p.Hq) {  // an fp16 cache: the chunk's values in half too
+          const uint16_t* vs = p.v_new + off[u];
+          uint16_t* vd = p.v_cvt + off[u];
+          *reinterpret_cast<uint4*>(vd + kc * 8) = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(vs + kc * 8)));
+          *reinterpret_cast<uint4*>(vd + D / 2 + kc * 8) =
+              bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(vs + D / 2 + kc * 8)));
+        }
+      } else {
+        rope_apply(lo[u], hi[u], tab);
+      }
       uint16_t* dst = (hh < p.Hq ? p.q_rot : p.k_rot) + off[u];
       *reinterpret_cast<uint4*>(dst + kc * 8) = lo[u];
       *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi[u];
@@ -279,8 +290,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) 
 }
 
 // SINK: the implicit mask also keeps pinned sink slots visible (a separate
-// instantiation, so the common case carries none of that code).
-template <int D, bool EXPLICIT, bool SINK>
+// instantiation, so the common case carries none of that code).  F16: an
+// fp16 KV cache, every product in fp16.
+template <int D, bool EXPLICIT, bool SINK, bool F16>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                      const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
@@ -381,8 +393,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(128, kBN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+      constexpr uint32_t idesc_qk = idesc_16(128, kBN, false, F16);
+      constexpr uint32_t idesc_pv = idesc_16(128, D, true, F16);
       const uint32_t q_addr = smem_u32(smem + CF::kQ);
       int g = 0, seg = 0;
       bool ok = true;
@@ -624,8 +636,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           for (int q = 0; q < 32; q += 4) {
             accA = fadd2(accA, make_float2(pv[q], pv[q + 1]));
             accB = fadd2(accB, make_float2(pv[q + 2], pv[q + 3]));
-            w[q / 2] = pack_bf16x2(pv[q], pv[q + 1]);
-            w[q / 2 + 1] = pack_bf16x2(pv[q + 2], pv[q + 3]);
+            w[q / 2] = pack16x2<F16>(pv[q], pv[q + 1]);
+            w[q / 2 + 1] = pack16x2<F16>(pv[q + 2], pv[q + 3]);
           }
           tmem_st16(s_col + 16 * c, w);
         }
@@ -859,14 +871,15 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
   w.ptag = off; off += al(static_cast<size_t>(ctas) * 2 * sizeof(int32_t));
   w.q_rot = off; off += al(static_cast<size_t>(B) * Hq * C * D * 2);
   w.k_rot = off; off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
+  w.v_cvt = off; off += al(static_cast<size_t>(B) * Hkv * C * D * 2);  // fp16 cache: chunk values in half
   w.total = off;
   return w;
 }
 
-template <int D, bool EXPLICIT, bool SINK = false>
+template <int D, bool EXPLICIT, bool SINK, bool F16>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   constexpr int smem = pair_smem_bytes<D>();
-  auto kern = attn_pair_kernel<D, EXPLICIT, SINK>;
+  auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -887,16 +900,17 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
                           stream, p);
 }
 
+template <int D, bool F16>
+static cudaError_t launch_pair_d(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+  if (p.mask) return launch_pair_t<D, true, false, F16>(maps, p, stream);
+  if (p.sink > 0) return launch_pair_t<D, false, true, F16>(maps, p, stream);
+  return launch_pair_t<D, false, false, F16>(maps, p, stream);
+}
+
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  const bool ex = p.mask != nullptr;
   switch (p.D) {
-    case 64:
-      return ex ? launch_pair_t<64, true>(maps, p, stream)
-                : (p.sink > 0 ? launch_pair_t<64, false, true>(maps, p, stream) : launch_pair_t<64, false>(maps, p, stream));
-    case 128:
-      return ex ? launch_pair_t<128, true>(maps, p, stream)
-                : (p.sink > 0 ? launch_pair_t<128, false, true>(maps, p, stream)
-                              : launch_pair_t<128, false>(maps, p, stream));
+    case 64: return p.f16 ? launch_pair_d<64, true>(maps, p, stream) : launch_pair_d<64, false>(maps, p, stream);
+    case 128: return p.f16 ? launch_pair_d<128, true>(maps, p, stream) : launch_pair_d<128, false>(maps, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

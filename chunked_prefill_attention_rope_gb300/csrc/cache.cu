@@ -29,7 +29,8 @@ __device__ __forceinline__ size_t crow(const CacheView& c, int b, int h, int s) 
   return static_cast<size_t>(b) * c.sb + static_cast<size_t>(h) * c.sh + static_cast<size_t>(s) * c.ss;
 }
 
-// Rotate K row i of the chunk (pair kc) and copy V row i, writing cache slot `dst`.
+// Rotate K row i of the chunk (pair kc) and copy V row i, writing cache slot `dst`
+// in the cache format (bf16, or half for an fp16 cache).
 __device__ __forceinline__ void put_new_row(const CacheView& c, const ChunkView& x, int b, int h, int i,
                                             int dst, int kc, int Hkv, int D, int C) {
   const size_t src = ((static_cast<size_t>(b) * Hkv + h) * C + i) * D;
@@ -37,12 +38,19 @@ __device__ __forceinline__ void put_new_row(const CacheView& c, const ChunkView&
   uint4 hi = ld16(x.k + src + D / 2 + kc * 8);
   const float* cr = x.cos + (static_cast<size_t>(b) * C + i) * D;
   const float* sr = x.sin + (static_cast<size_t>(b) * C + i) * D;
-  rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+  uint4 vl = ld16(x.v + src + kc * 8), vh = ld16(x.v + src + D / 2 + kc * 8);
+  if (c.f16) {
+    rope_pair<true>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+    vl = bf16x8_to_f16x8(vl);
+    vh = bf16x8_to_f16x8(vh);
+  } else {
+    rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+  }
   const size_t d = crow(c, b, h, dst);
   st16(c.k + d + kc * 8, lo);
   st16(c.k + d + D / 2 + kc * 8, hi);
-  st16(c.v + d + kc * 8, ld16(x.v + src + kc * 8));
-  st16(c.v + d + D / 2 + kc * 8, ld16(x.v + src + D / 2 + kc * 8));
+  st16(c.v + d + kc * 8, vl);
+  st16(c.v + d + D / 2 + kc * 8, vh);
 }
 
 __device__ __forceinline__ int clamp_rows(int n, int C, int32_t* err, bool report) {

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,6 +31,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Pack two fp32 values into an fp16x2 word (round to nearest even), lo first.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// The 16-bit operand format of the attention products: bf16, or fp16 for an
+// fp16 KV cache.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -199,12 +214,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format;
-//   bit 15 A major (0 = K); bit 16 B major (1 = MN); 17-22 N >> 3; 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor of kind::f16 with 16-bit A/B and fp32 D.
+//   bits 4-5 D format (1 = f32); 7-9 A format (0 = f16, 1 = bf16); 10-12 B
+//   format; bit 15 A major (0 = K); bit 16 B major (1 = MN); 17-22 N >> 3;
+//   24-28 M >> 4.  A and B always share one format.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return idesc_16(M, N, b_mn_major, false);
 }
 
 // tcgen05.ld, 32 lanes x 32 bits, 32 consecutive columns per thread.
@@ -377,6 +396,7 @@ __device__ __forceinline__ RopeTab rope_tab(const float* cos_lo, const float* si
 
 // Rotate one pair of 8-element bf16 chunks (dims d..d+7 and d+D/2..d+D/2+7)
 // with fp32 products and sums, no fused multiply-add, round to nearest even.
+template <bool F16 = false>
 __device__ __forceinline__ void rope_apply(uint4& lo, uint4& hi, const RopeTab& t) {
   const float4 cl0 = t.cl0, cl1 = t.cl1, sl0 = t.sl0, sl1 = t.sl1;
   const float4 ch0 = t.ch0, ch1 = t.ch1, sh0 = t.sh0, sh1 = t.sh1;
@@ -396,16 +416,24 @@ __device__ __forceinline__ void rope_apply(uint4& lo, uint4& hi, const RopeTab& 
     const float y1 = __fsub_rn(__fmul_rn(x1, cl[e1]), __fmul_rn(z1, sl[e1]));
     const float u0 = __fadd_rn(__fmul_rn(z0, chh[e0]), __fmul_rn(x0, shh[e0]));
     const float u1 = __fadd_rn(__fmul_rn(z1, chh[e1]), __fmul_rn(x1, shh[e1]));
-    ya[w] = pack_bf16x2(y0, y1);
-    yb[w] = pack_bf16x2(u0, u1);
+    ya[w] = pack16x2<F16>(y0, y1);
+    yb[w] = pack16x2<F16>(u0, u1);
   }
   lo = make_uint4(ya[0], ya[1], ya[2], ya[3]);
   hi = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
+template <bool F16 = false>
 __device__ __forceinline__ void rope_pair(uint4& lo, uint4& hi, const float* cos_lo, const float* sin_lo,
                                           const float* cos_hi, const float* sin_hi) {
-  rope_apply(lo, hi, rope_tab(cos_lo, sin_lo, cos_hi, sin_hi));
+  rope_apply<F16>(lo, hi, rope_tab(cos_lo, sin_lo, cos_hi, sin_hi));
+}
+
+// Eight bf16 values as eight fp16 values (nearest even; exact inside the
+// half range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                    pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
 }
 
 }  // namespace cpa

@@ -12,7 +12,8 @@
 //   * Warp 4 streams K and V tiles with TMA into a 3-stage ring (96 KB at
 //     D = 128, so two CTAs share an SM and keep ~190 KB of loads in flight).
 //   * Warps 0-3 each take 16 keys of every tile: S = Q K^T and O += P V with
-//     mma.sync m16n8k16 (bf16 in, fp32 accumulate), operands from the
+//     mma.sync m16n8k16 (bf16 in, or fp16 with an fp16 KV cache; fp32
+//     accumulate), operands from the
 //     swizzled tiles with ldmatrix.  Each warp keeps its own running max, sum
 //     and O; the four are merged through shared memory at the end.
 //
@@ -53,14 +54,24 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// C(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+// C(16x8, fp32) += A(16x16, row) * B(16x8, col), A and B bf16 (or fp16 for
+// an fp16 KV cache)
+template <bool F16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 // Byte offset of (row, 16-byte chunk c along D) in a tile stored as D/64
@@ -71,7 +82,7 @@ __device__ __forceinline__ uint32_t tile_off(int row, int c) {
 
 }  // namespace
 
-template <int D, bool EXPLICIT>
+template <int D, bool EXPLICIT, bool F16>
 __global__ void __launch_bounds__(kDThreads, 2)
     attn_decode_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                        const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
@@ -170,8 +181,8 @@ __global__ void __launch_bounds__(kDThreads, 2)
           const float u1 = __fadd_rn(__fmul_rn(z1, cr[d + D / 2 + 1]), __fmul_rn(x1, sr[d + D / 2 + 1]));
           // register slot: a0 (row r0, cols c2), a1 (row r0+8, c2), a2 (row r0, c2+8), a3 (row r0+8, c2+8)
           const int slot = half + 2 * hi8;
-          qa[k][slot] = pack_bf16x2(y0, y1);
-          qa[k + KS / 2][slot] = pack_bf16x2(u0, u1);
+          qa[k][slot] = pack16x2<F16>(y0, y1);
+          qa[k + KS / 2][slot] = pack16x2<F16>(u0, u1);
         }
       }
     }
@@ -218,9 +229,16 @@ __global__ void __launch_bounds__(kDThreads, 2)
         uint4 lo = *plo, hi = *phi;
         const float* cr = p.cos + (static_cast<size_t>(b) * p.C + base + r) * D;
         const float* sr = p.sin + (static_cast<size_t>(b) * p.C + base + r) * D;
-        rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+        rope_pair<F16>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
         *plo = lo;
         *phi = hi;
+        if (F16) {  // the chunk's values, bf16 -> half, in place
+          uint8_t* vtile = smem + CF::kV + st * CF::kTile;
+          uint4* qlo = reinterpret_cast<uint4*>(vtile + tile_off(r, kc));
+          uint4* qhi = reinterpret_cast<uint4*>(vtile + tile_off(r, kh));
+          *qlo = bf16x8_to_f16x8(*qlo);
+          *qhi = bf16x8_to_f16x8(*qhi);
+        }
       }
       fence_async_smem();  // the ring slot is refilled by TMA later
       asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -234,8 +252,8 @@ __global__ void __launch_bounds__(kDThreads, 2)
       const int row = key0 + (mtx >> 1) * 8 + (lane & 7);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(kt + tile_off(row, 2 * k + (mtx & 1)), b0, b1, b2, b3);
-      mma16816(s[0], qa[k][0], qa[k][1], qa[k][2], qa[k][3], b0, b1);
-      mma16816(s[1], qa[k][0], qa[k][1], qa[k][2], qa[k][3], b2, b3);
+      mma16816<F16>(s[0], qa[k][0], qa[k][1], qa[k][2], qa[k][3], b0, b1);
+      mma16816<F16>(s[1], qa[k][0], qa[k][1], qa[k][2], qa[k][3], b2, b3);
     }
 
     // scores -> masked log2-domain values; this thread holds rows r0 (idx 0,1) and r0+8 (idx 2,3)
@@ -303,7 +321,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
           }
         }
         psum[hf] = __fadd_rn(psum[hf], __fadd_rn(pv[0], pv[1]));
-        pa[hf + 2 * nb] = pack_bf16x2(pv[0], pv[1]);
+        pa[hf + 2 * nb] = pack16x2<F16>(pv[0], pv[1]);
       }
     }
 #pragma unroll
@@ -322,8 +340,8 @@ __global__ void __launch_bounds__(kDThreads, 2)
       const int row = key0 + (mtx & 1) * 8 + (lane & 7);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(vt + tile_off(row, 2 * n2 + (mtx >> 1)), b0, b1, b2, b3);
-      mma16816(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-      mma16816(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      mma16816<F16>(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
+      mma16816<F16>(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->empty[st]);
@@ -402,10 +420,10 @@ __global__ void __launch_bounds__(kDThreads, 2)
   if (threadIdx.x == 0 && bars->abort) set_err(p.err, CPA_EBIT_TIMEOUT);
 }
 
-template <int D, bool EXPLICIT>
+template <int D, bool EXPLICIT, bool F16>
 static cudaError_t launch_decode_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   using CF = DecCfg<D>;
-  auto kern = attn_decode_kernel<D, EXPLICIT>;
+  auto kern = attn_decode_kernel<D, EXPLICIT, F16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
@@ -417,11 +435,17 @@ static cudaError_t launch_decode_t(const CUtensorMap* maps, const AttnParams& p,
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+template <int D>
+static cudaError_t launch_decode_d(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   const bool ex = p.mask != nullptr;
+  if (p.f16) return ex ? launch_decode_t<D, true, true>(maps, p, stream) : launch_decode_t<D, false, true>(maps, p, stream);
+  return ex ? launch_decode_t<D, true, false>(maps, p, stream) : launch_decode_t<D, false, false>(maps, p, stream);
+}
+
+cudaError_t launch_attn_decode(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   switch (p.D) {
-    case 64: return ex ? launch_decode_t<64, true>(maps, p, stream) : launch_decode_t<64, false>(maps, p, stream);
-    case 128: return ex ? launch_decode_t<128, true>(maps, p, stream) : launch_decode_t<128, false>(maps, p, stream);
+    case 64: return launch_decode_d<64>(maps, p, stream);
+    case 128: return launch_decode_d<128>(maps, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

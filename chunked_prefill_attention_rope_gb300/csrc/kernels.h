@@ -56,6 +56,8 @@ struct AttnParams {
   uint16_t* q_rot;        // rotated queries [B, Hq, C, D] (workspace)
   uint16_t* k_rot;        // rotated chunk keys [B, Hkv, C, D] (workspace)
   int32_t* ptag;          // [2 * ctas] unit of each CTA's partial slots (-1: none)
+  int f16;                // fp16 KV cache: every product runs in fp16 (else bf16)
+  uint16_t* v_cvt;        // fp16 KV cache: the chunk values in fp16 (workspace)
   int cluster;            // single-tile path: the splits of a query tile form one
                           // thread-block cluster and merge their partials in-kernel
   // Fused global append (app_n non-null): the rotated chunk keys and the
@@ -77,7 +79,7 @@ struct PairTeams {
 };
 PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms);
 struct PairWorkspace {
-  size_t ustart, part_o, part_lse, ptag, q_rot, k_rot, total;
+  size_t ustart, part_o, part_lse, ptag, q_rot, k_rot, v_cvt, total;
 };
 PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t);
 // maps for the pair path: cache K, cache V, rotated chunk K, chunk V, rotated Q
@@ -109,6 +111,7 @@ struct CacheView {
   int64_t sb, sh, ss;  // strides in elements
   int32_t* len;
   int cap, window, sink;
+  int f16;  // elements are IEEE half (else bf16)
 };
 
 struct ChunkView {

@@ -118,9 +118,14 @@ __device__ __forceinline__ void fused_append_pair(const AttnParams& p, int b, in
   const size_t src = ((static_cast<size_t>(b) * p.Hkv + h) * p.C + i) * D;
   *reinterpret_cast<uint4*>(p.app_k + dst + kc * 8) = lo;
   *reinterpret_cast<uint4*>(p.app_k + dst + D / 2 + kc * 8) = hi;
-  *reinterpret_cast<uint4*>(p.app_v + dst + kc * 8) = *reinterpret_cast<const uint4*>(p.v_new + src + kc * 8);
-  *reinterpret_cast<uint4*>(p.app_v + dst + D / 2 + kc * 8) =
-      *reinterpret_cast<const uint4*>(p.v_new + src + D / 2 + kc * 8);
+  uint4 vl = *reinterpret_cast<const uint4*>(p.v_new + src + kc * 8);
+  uint4 vh = *reinterpret_cast<const uint4*>(p.v_new + src + D / 2 + kc * 8);
+  if (p.f16) {  // an fp16 cache: the rotated keys are half already; convert the values
+    vl = bf16x8_to_f16x8(vl);
+    vh = bf16x8_to_f16x8(vh);
+  }
+  *reinterpret_cast<uint4*>(p.app_v + dst + kc * 8) = vl;
+  *reinterpret_cast<uint4*>(p.app_v + dst + D / 2 + kc * 8) = vh;
 }
 
 // Fused append: advance len (or flag the sequence that has no room); one

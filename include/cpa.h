@@ -60,6 +60,9 @@ typedef enum {
 #define CPA_EBIT_TIMEOUT 32       /* a bounded in-kernel pipeline wait ran out */
 
 enum { CPA_CACHE_GLOBAL = 0, CPA_CACHE_SLIDING = 1 };
+/* Element format of a cache's K and V ([P4, Declined with rationale] names a
+ * runtime option that keeps the KV cache in fp16). */
+enum { CPA_KV_BF16 = 0, CPA_KV_F16 = 1 };
 
 /*
  * A KV cache for one layer.  Element (b, h, s, d) of K (and of V) lives at
@@ -71,6 +74,12 @@ enum { CPA_CACHE_GLOBAL = 0, CPA_CACHE_SLIDING = 1 };
  *           overflows evicts the oldest non-sink rows and compacts.
  * Rows at or beyond len[b] are dead: the library never promises their bytes
  * ([P4, Declined with rationale]: nothing reads past the length).
+ * dtype CPA_KV_F16: K and V hold IEEE half values.  Appends round the fp32
+ * rotation of each key (the same arithmetic as for bf16) to half, nearest
+ * even, and convert value rows bf16 -> half (exact inside the half range;
+ * larger values become infinite).  The attention then runs its products in
+ * fp16: Q and the chunk keys are rotated to half, the chunk values and P are
+ * half, accumulation is fp32 and the output stays bf16.
  */
 typedef struct {
   void* k;
@@ -81,6 +90,7 @@ typedef struct {
   int32_t kind;     /* CPA_CACHE_GLOBAL or CPA_CACHE_SLIDING */
   int32_t window;   /* SLIDING: W rows (<= cap); GLOBAL: ignored */
   int32_t sink;     /* SLIDING: S pinned rows; GLOBAL: ignored */
+  int32_t dtype;    /* CPA_KV_BF16 or CPA_KV_F16 */
 } cpa_cache;
 
 /*

@@ -58,17 +58,25 @@ def cache_bytes(t: torch.Tensor) -> np.ndarray:
     return bf16_bits(t)
 
 
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """Raw 16-bit patterns (bf16 or fp16 tensors) as a uint16 numpy array."""
+    assert t.dtype in (torch.bfloat16, torch.float16)
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def oracle_attn(q, k_new, v_new, cos, sin, ck, cv, P, past_len, n_real, window=0, causal=1,
                 mask=None, sel_row=None, sink=0):
-    """Run the oracle on host copies of torch tensors."""
+    """Run the oracle on host copies of torch tensors (the cache format follows
+    the cache tensors' dtype)."""
     f = lambda t: None if t is None else t.detach().cpu()
     L = f(past_len).numpy() if past_len is not None else None
     n = f(n_real).numpy() if n_real is not None else None
     m = None if mask is None else f(mask).numpy()
     s = None if sel_row is None else f(sel_row).numpy()
+    kv = "f16" if ck.dtype == torch.float16 else "bf16"
     return O.chunk_prefill_attn(bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new), f(cos).numpy(),
-                                f(sin).numpy(), bf16_bits(ck), bf16_bits(cv), P, L, n,
-                                window=window, causal=causal, mask=m, sel_row=s, sink=sink)
+                                f(sin).numpy(), bits16(ck), bits16(cv), P, L, n,
+                                window=window, causal=causal, mask=m, sel_row=s, sink=sink, kv=kv)
 
 
 def explicit_masks(past_len, n_real, C, P, Hq, window, causal, sink=0):
