@@ -373,6 +373,7 @@ def ours(args, rank, world, dev):
     if not args.no_tail_policy:
         line["tail_policy"] = measure_tail_policy(cpa, dev)
         line["page1"] = measure_page1(cpa, dev)
+        line["f16_cache"] = measure_f16_cache(cpa, parts, dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(parts, tokens, budget_s=args.cpu_seconds)
     return line
@@ -480,6 +481,48 @@ def measure_tail_policy(cpa, dev, tails=TAIL_TAILS):
             "timing": "one CUDA graph per sequence, median of 20 replays, L2-resident",
             "crossover_c128": crossover("padded_c128_us"), "crossover_bucket": crossover("padded_bucket_us"),
             "rows": rows}
+
+
+# ------------------------------------------------------------------ fp16 KV cache
+
+def measure_f16_cache(cpa, parts, dev, reps=10):
+    """The long-context attention call and the decode call over fp16 copies of
+    the same caches (CPA_KV_F16: every product in fp16); CUDA events, median of
+    `reps`, inputs larger than L2."""
+    res = {}
+    for key, name in (("prefill", "long_context_attn"), ("decode", "decode_attn")):
+        pt = parts[key]
+        i = pt.inp
+        cache = cpa.KVCache(pt.cache.k.to(torch.float16), pt.cache.v.to(torch.float16), pt.len0.clone())
+        err = cpa.new_error_word(dev)
+        call = cpa.decode_step if key == "decode" else cpa.chunk_prefill_attn
+
+        def f():
+            call(i["q"], i["k"], i["v"], i["cos"], i["sin"], cache, pt.w.P, past_len=i["past_len"],
+                 n_real=i["n_real"], out=pt.out, workspace=pt.ws, err=err)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        if int(err[0]) != 0:
+            raise RuntimeError(f"fp16 cache: device error bits {int(err[0])}")
+        ms = statistics.median(ts)
+        res[name + "_ms"] = round(ms, 4)
+        if key == "prefill":
+            res[name + "_tflops"] = round(pt.flops / (ms * 1e-3) / 1e12, 1)
+        else:
+            res[name + "_kv_gbs"] = round(pt.bytes / (ms * 1e-3) / 1e9, 1)
+        del cache
+        torch.cuda.empty_cache()
+    res["note"] = "same workloads as parts, caches converted to fp16 (CPA_KV_F16)"
+    return res
 
 
 # ------------------------------------------------------------------ page-1 call shape
