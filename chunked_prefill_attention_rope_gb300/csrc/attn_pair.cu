@@ -179,7 +179,7 @@ struct SegWalk {
 }  // namespace
 
 constexpr int kPrepThreads = 256;
-constexpr int kPrepHeads = 8;  // heads rotated per item with one table load
+constexpr int kPrepHeads = 4;  // heads rotated per item with one table load (two CTAs per SM)
 
 // Cost of every block (its live key tiles plus the switch cost) and the
 // exclusive prefix sum of the costs, by one CTA of kPrepThreads threads.
@@ -226,11 +226,11 @@ __device__ void plan_units(const AttnParams& p) {
 
 // The last CTA plans (plan_units); the others rotate the chunk's queries and
 // keys into the workspace.  An item is one (sequence, chunk row, chunk pair)
-// and up to eight heads of the combined list [query heads, key heads]: the
-// table values of its row are loaded once and the eight heads' loads are
+// and up to four heads of the combined list [query heads, key heads]: the
+// table values of its row are loaded once and the four heads' loads are
 // issued together.  A warp covers four consecutive rows of each head, so
 // every load and store is a contiguous 512-byte run per head.
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams p) {
   grid_launch_dependents();
   if (blockIdx.x == gridDim.x - 1) {
     plan_units(p);
