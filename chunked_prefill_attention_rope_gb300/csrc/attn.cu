@@ -35,9 +35,11 @@
 //               Rotates the TMA-loaded Q rows in shared memory at the start,
 //               applies the mask, keeps the running
 //               max / sum in fp32 (log2 domain, rescaling O only when the max
-//               grows by more than 2^8), writes P as bf16, and finally scales
-//               O by 1/l into a shared-memory staging tile, from which whole
-//               rows are stored (or merged) with coalesced accesses.
+//               grows by more than 2^8), writes P as bf16 (fp16 for an fp16
+//               KV cache), and finally scales O by 1/l: into a shared-memory
+//               staging tile from which whole rows are stored with coalesced
+//               accesses, or, in a cluster, straight into the slice owner's
+//               shared memory.
 #include "tiles.cuh"
 
 namespace cpa {
