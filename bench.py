@@ -374,6 +374,7 @@ def ours(args, rank, world, dev):
         line["tail_policy"] = measure_tail_policy(cpa, dev)
         line["page1"] = measure_page1(cpa, dev)
         line["f16_cache"] = measure_f16_cache(cpa, parts, dev)
+        line["explicit_mask"] = measure_explicit_mask(cpa, dev, hbm)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(parts, tokens, budget_s=args.cpu_seconds)
     return line
@@ -525,19 +526,75 @@ def measure_f16_cache(cpa, parts, dev, reps=10):
     return res
 
 
+def measure_explicit_mask(cpa, dev, hbm_gbs, reps=10):
+    """The packed batch (16 sequences, 32/8 heads, D 128, C 128, past uniform
+    on [0, 4095]) with its mask passed explicitly as a [16, 32, 128, 4224] fp32
+    tensor (1.1 GB) and, for comparison, implicitly; CUDA events, median of
+    `reps`, the mask larger than L2.  The explicit call visits every key tile,
+    so its bytes are the whole mask plus every cache row's keys and values."""
+    w = WORKLOADS["packed_batch"]
+    inp = make_chunk_inputs(w, device=dev)
+    ck, cv = make_cache(w, device=dev)
+    cache = cpa.KVCache(ck, cv, inp["past_len"].clone())
+    mask = batch_mask(w, inp["past_len"].cpu(), inp["n_real"].cpu(), dev)
+    out = torch.empty((w.B, w.Hq, w.C, w.D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)), dtype=torch.uint8,
+                     device=dev)
+    err = cpa.new_error_word(dev)
+    res = {}
+    for tag, m in (("implicit", None), ("explicit", mask)):
+        def f():
+            cpa.chunk_prefill_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], cache, w.P,
+                                   past_len=inp["past_len"], n_real=inp["n_real"], mask=m, out=out, workspace=ws,
+                                   err=err)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        res[tag + "_ms"] = round(statistics.median(ts), 4)
+    if int(err[0]) != 0:
+        raise RuntimeError(f"explicit mask: device error bits {int(err[0])}")
+    mask_bytes = mask.numel() * 4
+    kv_bytes = 2 * w.B * w.Hkv * (w.P + w.C) * w.D * 2
+    qo_bytes = 2 * w.B * w.Hq * w.C * w.D * 2
+    gbs = (mask_bytes + kv_bytes + qo_bytes) / (res["explicit_ms"] * 1e-3) / 1e9
+    res.update({"workload": "packed batch B16, 32/8 heads, D128, C128, past U[0, 4095], fp32 mask [16, 32, 128, 4224]",
+                "explicit_bytes": mask_bytes + kv_bytes + qo_bytes, "explicit_gbs": round(gbs, 1),
+                "explicit_frac_of_hbm": round(gbs / hbm_gbs, 3)})
+    del mask, cache, ck, cv
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ page-1 call shape
 
-def additive_mask(L, n, C, P, Hq, W):
+def additive_mask(L, n, C, P, Hq, W, device=None):
     """[1, Hq, C, P+C] fp32 additive mask of one sequence: 0 where the key is
     visible (past slot j < L within the window, chunk row t < n with t <= i
     within the window), -1e30 elsewhere."""
-    i = torch.arange(C)[:, None]
-    j = torch.arange(P + C)[None, :]
+    i = torch.arange(C, device=device)[:, None]
+    j = torch.arange(P + C, device=device)[None, :]
     t = j - P
     in_win = lambda d: torch.ones_like(d, dtype=torch.bool) if W == 0 else d < W
     vis = torch.where(j < P, (j < L) & in_win(L + i - j), (t < n) & (t <= i) & in_win(i - t))
-    m = torch.where(vis, torch.tensor(0.0), torch.tensor(-1e30)).to(torch.float32)
+    m = torch.where(vis, 0.0, -1e30).to(torch.float32)
     return m[None, None].expand(1, Hq, C, P + C).contiguous()
+
+
+def batch_mask(w, L, n, device):
+    """[B, Hq, C, P+C] explicit mask equal to the implicit one of workload `w`
+    (causal, its window) for past lengths L and real rows n.  Global caches
+    only: in a sliding cache, slots are not positions."""
+    if getattr(w, "kind", "global") != "global":
+        raise ValueError("explicit masks here are built for global caches")
+    return torch.cat([additive_mask(int(L[b]), int(n[b]), w.C, w.P, w.Hq, w.window, device) for b in range(w.B)])
 
 
 def measure_page1(cpa, dev, reps=10):
@@ -701,9 +758,10 @@ def reference(args, rank, world):
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def run_case(name, reps, batch=None):
+def run_case(name, reps, batch=None, explicit=False):
     """Run one workload's attention call `reps` times on cuda:0 (for profiler
-    captures: the n-th launch of a kernel is the n-th call)."""
+    captures: the n-th launch of a kernel is the n-th call); `explicit` passes
+    the workload's mask as an explicit [B, Hq, C, P+C] tensor."""
     import dataclasses
     import chunked_prefill_attention_rope_gb300 as cpa
     from chunked_prefill_attention_rope_gb300.build import build
@@ -719,14 +777,15 @@ def run_case(name, reps, batch=None):
     need = cpa.attn_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.C, w.P)
     ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
     err = cpa.new_error_word(dev)
+    mask = batch_mask(w, inp["past_len"].cpu(), inp["n_real"].cpu(), dev) if explicit else None
     f = cpa.decode_step if w.C == 1 else cpa.chunk_prefill_attn
     for _ in range(reps):
         f(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], cache, w.P, past_len=inp["past_len"],
-          n_real=inp["n_real"], window=w.window, causal=bool(w.causal), out=out, workspace=ws, err=err)
+          n_real=inp["n_real"], window=w.window, causal=bool(w.causal), mask=mask, out=out, workspace=ws, err=err)
     torch.cuda.synchronize()
     if int(err[0]) != 0:
         raise RuntimeError(f"device error bits {int(err[0])}")
-    print(json.dumps({"case": name, "B": w.B, "reps": reps, "ok": True}))
+    print(json.dumps({"case": name, "B": w.B, "reps": reps, "explicit_mask": explicit, "ok": True}))
 
 
 def main():
@@ -741,9 +800,10 @@ def main():
     ap.add_argument("--case", default=None, help="run only this workload's attention call (profiling)")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--explicit-mask", action="store_true", help="with --case: pass the mask explicitly")
     args = ap.parse_args()
     if args.case:
-        run_case(args.case, args.reps, args.batch)
+        run_case(args.case, args.reps, args.batch, args.explicit_mask)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

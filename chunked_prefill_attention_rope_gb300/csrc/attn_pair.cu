@@ -70,6 +70,11 @@ struct PairCfg {
   static constexpr int kBars = kV + kStages * kVBytes;
   static constexpr int kOCol = 2 * kBN;  // O0 at [256, 256 + D), O1 at [256 + D, 256 + 2D)
   static_assert(kOCol + 2 * D <= 512, "TMEM columns");
+  // explicit mask only: a 32-row x 32-key fp32 staging tile per softmax warp,
+  // then each warp's 32 mask-row indices
+  static constexpr int kMaskStage = kBars + 256;
+  static constexpr int kMaskRows = kMaskStage + 8 * 32 * 32 * 4;
+  static constexpr int kMaskEnd = kMaskRows + 8 * 32 * 4;
 };
 
 struct __align__(8) PairBars {
@@ -80,10 +85,12 @@ struct __align__(8) PairBars {
   int abort;
 };
 
-template <int D>
+template <int D, bool EXPLICIT>
 constexpr int pair_smem_bytes() {
-  return PairCfg<D>::kBars + static_cast<int>(sizeof(PairBars)) + 1024;
+  static_assert(sizeof(PairBars) <= 256, "barrier block");
+  return (EXPLICIT ? PairCfg<D>::kMaskEnd : PairCfg<D>::kBars + static_cast<int>(sizeof(PairBars))) + 1024;
 }
+static_assert(pair_smem_bytes<128, true>() <= 227 * 1024, "shared memory");
 
 struct Unit {
   int b, kvh, pair;
@@ -286,6 +293,67 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
       *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi[u];
       if (p.app_n && hh >= p.Hq) fused_append_pair(p, b, hh - p.Hq, i, kc, lo[u], hi[u]);
     }
+  }
+}
+
+// Explicit mask values of keys [k0, k0 + 32) of a tile for this thread's row
+// (`mp`: the row at the tile's first key, or null), one value at a time, -1e30
+// at or past `lim`: the path for P or C not a multiple of 4.
+__device__ __forceinline__ void load_mask32(float (&mv)[32], const float* mp, int k0, int lim) {
+#pragma unroll
+  for (int q = 0; q < 32; ++q) mv[q] = (mp && k0 + q < lim) ? __ldg(mp + k0 + q) : -1e30f;
+}
+
+// Explicit mask values of keys [k0, k0 + 32) of a tile for the 32 rows of one
+// warp, read coalesced: eight loads of 16 bytes per lane, lane l taking keys
+// k0 + 4 (l % 8) of rows 4 k + l / 8, so that four rows share one load
+// instruction.  `rows` holds the warp's mask-row indices (-1: none) in the
+// order row % 4, row / 4; `moff` is the tile's first key in the mask row and
+// keys at or past `lim` read -1e30.  Needs P and C multiples of 4, so that no
+// vector straddles `lim`.
+__device__ __forceinline__ void fetch_mask32(float4 (&v)[8], const float* mask, size_t stride, const int* rows,
+                                             int lane, size_t moff, int k0, int lim) {
+  const int4 ra = reinterpret_cast<const int4*>(rows)[(lane >> 3) * 2];
+  const int4 rb = reinterpret_cast<const int4*>(rows)[(lane >> 3) * 2 + 1];
+  const int ridx[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+  const int col = lane & 7;
+  const bool in = k0 + 4 * col < lim;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = make_float4(-1e30f, -1e30f, -1e30f, -1e30f);
+    if (in && ridx[k] >= 0)
+      v[k] = __ldg(reinterpret_cast<const float4*>(mask + static_cast<size_t>(ridx[k]) * stride + moff + k0 + 4 * col));
+  }
+}
+
+// Where tile `t` of the plan starts in a mask row (`moff`) and how many of
+// its keys the row holds (`lim`: keys at or past it are outside the row).
+__device__ __forceinline__ void mask_span(const AttnParams& p, const TilePlan& tp, int t, size_t& moff, int& lim) {
+  const bool chunk = t < tp.Tc;
+  const int base = (chunk ? t : t - tp.Tc) * kBN;
+  lim = chunk ? p.C - base : p.P - base;
+  moff = chunk ? static_cast<size_t>(p.P) + base : static_cast<size_t>(base);
+}
+
+// The values fetch_mask32 read, handed to the lane that owns each row through
+// the warp's staging tile (16-byte slots XOR-swizzled by row, so neither the
+// stores nor the loads have bank conflicts).
+__device__ __forceinline__ void deal_mask32(float (&mv)[32], const float4 (&v)[8], float4* stg, int lane) {
+  const int col = lane & 7;
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = 4 * k + (lane >> 3);
+    stg[r * 8 + (col ^ (r & 7))] = v[k];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 x = stg[lane * 8 + (k ^ (lane & 7))];
+    mv[4 * k] = x.x;
+    mv[4 * k + 1] = x.y;
+    mv[4 * k + 2] = x.z;
+    mv[4 * k + 3] = x.w;
   }
 }
 
@@ -498,6 +566,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t s_col = tmem + lanes + qi * kBN;
     const uint32_t o_col = tmem + lanes + CF::kOCol + qi * D;
     const float sl2 = p.sl2;
+    // explicit mask staging (only allocated for the explicit instantiation)
+    float4* mstage = reinterpret_cast<float4*>(smem + CF::kMaskStage) + warp * 32 * 8;
+    int* mrows = reinterpret_cast<int*>(smem + CF::kMaskRows) + warp * 32;
     int g = 0, seg = 0;
     bool ok = true;
     int unit, a, e;
@@ -513,11 +584,20 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 
       RowSpan span;
       span.init(p, tp, i, valid);
+      const bool mask_vec = (p.P % 4 == 0) && (p.C % 4 == 0);
+      const size_t mstride = static_cast<size_t>(p.P + p.C);
       const float* mrow = nullptr;
-      if (EXPLICIT && valid)
-        mrow = p.mask + ((static_cast<size_t>(x.b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C);
+      if (EXPLICIT) {
+        const int ridx = valid ? (x.b * p.Hq + h) * p.C + i : -1;
+        if (valid) mrow = p.mask + static_cast<size_t>(ridx) * mstride;
+        __syncwarp();
+        mrows[(lane & 3) * 8 + (lane >> 2)] = ridx;
+        __syncwarp();
+      }
       float m_run = kMaskedLog2, l_run = 0.f;
       const int n = e - a;
+      float4 fq[2][8];          // explicit mask: two chunks in flight
+      bool mask_ahead = false;  // fq already holds this tile's first two chunks
       for (int jj = 0; jj < n; ++jj) {
         const int gt = g + jj;
         const int t = tp.index(a + jj);
@@ -527,9 +607,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         span.tile(chunk, base, lo, hi, sk);
         const float* mp = nullptr;
         int lim = 0;
+        size_t moff = 0;
         if (EXPLICIT) {
-          lim = chunk ? p.C - base : p.P - base;
-          if (mrow) mp = mrow + (chunk ? p.P + base : base);
+          mask_span(p, tp, t, moff, lim);
+          if (mrow) mp = mrow + moff;
         }
         if (!(ok = warp_all(mbar_wait(&bars->s_full[qi], gt & 1, abort)))) break;
         tc_fence_after();
@@ -572,16 +653,58 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           m_tile = (mt == -INFINITY) ? kMaskedLog2 : __fmul_rn(mt, sl2);
         } else {
           float mt = -INFINITY;
+          // t = scale*log2e*s + log2e*mask, chunk by chunk (the mask fetched
+          // two chunks ahead and dealt out), written back over S for the
+          // exponentials below; the row max of t on the way.
+          if (mask_vec && !mask_ahead) {
+            fetch_mask32(fq[0], p.mask, mstride, mrows, lane, moff, 0, lim);
+            fetch_mask32(fq[1], p.mask, mstride, mrows, lane, moff, 32, lim);
+          }
+          float mt0 = -INFINITY, mt1 = -INFINITY;
 #pragma unroll
           for (int c = 0; c < kBN / 32; ++c) {
+            float mc[32];
+            if (mask_vec) {
+              deal_mask32(mc, fq[c & 1], mstage, lane);
+              if (c + 2 < kBN / 32) fetch_mask32(fq[c & 1], p.mask, mstride, mrows, lane, moff, 32 * (c + 2), lim);
+            } else {
+              load_mask32(mc, mp, 32 * c, lim);
+            }
             uint32_t r[32];
             tmem_ld32(s_col + 32 * c, r);
             tmem_ld_wait(r);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int k = 32 * c + q;
-              const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
-              mt = fmaxf(mt, __fmaf_rn(__uint_as_float(r[q]), sl2, __fmul_rn(mv, kLog2e)));
+            for (int q = 0; q < 32; q += 4) {
+              const float2 lo2 = ffma2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])),
+                                       make_float2(sl2, sl2),
+                                       fmul2(make_float2(mc[q], mc[q + 1]), make_float2(kLog2e, kLog2e)));
+              const float2 hi2 = ffma2(make_float2(__uint_as_float(r[q + 2]), __uint_as_float(r[q + 3])),
+                                       make_float2(sl2, sl2),
+                                       fmul2(make_float2(mc[q + 2], mc[q + 3]), make_float2(kLog2e, kLog2e)));
+              mt0 = fmax3(mt0, lo2.x, lo2.y);
+              mt1 = fmax3(mt1, hi2.x, hi2.y);
+              r[q] = __float_as_uint(lo2.x);
+              r[q + 1] = __float_as_uint(lo2.y);
+              r[q + 2] = __float_as_uint(hi2.x);
+              r[q + 3] = __float_as_uint(hi2.y);
+            }
+            tmem_st32(s_col + 32 * c, r);
+          }
+          tmem_st_wait();
+          mt = fmaxf(mt0, mt1);
+          // the next tile's first two chunks load (and its last two move to
+          // L2) while this tile's exponentials run and its next S is made
+          mask_ahead = mask_vec && jj + 1 < n;
+          if (mask_ahead) {
+            size_t moff1;
+            int lim1;
+            mask_span(p, tp, tp.index(a + jj + 1), moff1, lim1);
+            fetch_mask32(fq[0], p.mask, mstride, mrows, lane, moff1, 0, lim1);
+            fetch_mask32(fq[1], p.mask, mstride, mrows, lane, moff1, 32, lim1);
+            if (mrow) {
+#pragma unroll
+              for (int k = 64; k < kBN; k += 32)
+                if (k < lim1) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(mrow + moff1 + k)));
             }
           }
           m_tile = mt;
@@ -608,29 +731,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
         // P = 2^(scale*log2e*s - m), summed in one fixed order, written over S as bf16
         float2 accA = make_float2(0.f, 0.f), accB = accA;
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          float* pv = sc + 32 * c;
-          if (!EXPLICIT) {
-            const float nm = live ? -m_run : -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const float2 y = ffma2(make_float2(pv[q], pv[q + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-              pv[q] = fast_exp2(y.x);
-              pv[q + 1] = fast_exp2(y.y);
-            }
-          } else {
-            uint32_t r[32];
-            tmem_ld32(s_col + 32 * c, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int k = 32 * c + q;
-              const float mv = (mp && k < lim) ? __ldg(mp + k) : -1e30f;
-              pv[q] = live ? fast_exp2(__fmaf_rn(__uint_as_float(r[q]), sl2, __fadd_rn(__fmul_rn(mv, kLog2e), -m_run)))
-                           : 0.f;
-            }
-          }
+        auto emit = [&](const float* pv, int c) {
           uint32_t w[16];
 #pragma unroll
           for (int q = 0; q < 32; q += 4) {
@@ -640,6 +741,37 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             w[q / 2 + 1] = pack16x2<F16>(pv[q + 2], pv[q + 3]);
           }
           tmem_st16(s_col + 16 * c, w);
+        };
+        if (!EXPLICIT) {
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            float* pv = sc + 32 * c;
+            const float nm = live ? -m_run : -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const float2 y = ffma2(make_float2(pv[q], pv[q + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+              pv[q] = fast_exp2(y.x);
+              pv[q + 1] = fast_exp2(y.y);
+            }
+            emit(pv, c);
+          }
+        } else {
+          // P = 2^(t - m) from the t written above
+          const float nm = live ? -m_run : -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(s_col + 32 * c, r);
+            tmem_ld_wait(r);
+            float pv[32];
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const float2 y = fadd2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), make_float2(nm, nm));
+              pv[q] = fast_exp2(y.x);
+              pv[q + 1] = fast_exp2(y.y);
+            }
+            emit(pv, c);
+          }
         }
         const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
         tmem_st_wait();
@@ -878,7 +1010,7 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
 
 template <int D, bool EXPLICIT, bool SINK, bool F16>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  constexpr int smem = pair_smem_bytes<D>();
+  constexpr int smem = pair_smem_bytes<D, EXPLICIT>();
   auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16>;
   static bool attr_set = false;
   if (!attr_set) {

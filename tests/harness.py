@@ -38,6 +38,29 @@ def assert_close(gpu_bf16, ref, what=""):
     return max_abs, rel
 
 
+def two_tile_path(D, Hq, Hkv, C):
+    """True when the library serves these sizes with the persistent two-tile
+    kernel: D 64 or 128, at least two 128-row query tiles of (head, row) pairs,
+    and not the one-token decode kernel (C = 1, at most 16 heads per group)."""
+    G = Hq // Hkv
+    nq = -(-C // max(1, 128 // G))
+    decode = C == 1 and D in (64, 128) and G <= 16
+    return D in (64, 128) and nq >= 2 and not decode
+
+
+def assert_explicit_matches(out_e, out_i, two_tile, what=""):
+    """Outputs of the explicit and the implicit form of one mask: bitwise
+    identical, except on the two-tile kernel, whose explicit path rounds the
+    masked, scaled score once before the row max is subtracted where the
+    implicit path fuses both steps: there within rounding."""
+    if not two_tile:
+        assert torch.equal(out_e.view(torch.int16), out_i.view(torch.int16)), f"{what}: explicit != implicit"
+        return
+    ref = out_i.detach().float().cpu().numpy().astype(np.float64)
+    max_abs, rel = compare(out_e, ref, what)
+    assert max_abs <= MAX_ABS and rel <= 1e-3, f"{what}: explicit vs implicit max_abs={max_abs:.3e} rel_l2={rel:.3e}"
+
+
 def check_argmax(gpu_sel: torch.Tensor, ref_sel: np.ndarray, what=""):
     """Selected-row argmax: exact when the oracle's top-2 gap exceeds ARGMAX_GAP;
     otherwise the GPU's pick must be one of the near-tied oracle maxima."""

@@ -7,7 +7,8 @@ convert values to half (bit-exact against the oracle, global and sliding,
 through a padded tail with snapshot and rollback); the attention runs its
 products in fp16 on every path (two-tile, single-tile with and without a
 cluster, decode, explicit mask, fused append) and matches the oracle within
-the attention tolerance; explicit and implicit masks give the same bits.
+the attention tolerance; explicit and implicit masks give the same bits
+(within rounding on the two-tile kernel).
 """
 import numpy as np
 import pytest
@@ -15,7 +16,8 @@ import torch
 
 import oracle as O
 from synth import Workload, make_chunk_inputs, make_cache, normal_bf16, rope_tables, bf16_bits, uniform_int
-from harness import lib, assert_close, check_argmax, oracle_attn, explicit_masks, bits16
+from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks, bits16, two_tile_path,
+                     assert_explicit_matches)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -62,7 +64,8 @@ def test_f16_cache_attention_matches_oracle(w):
     check_argmax(sel, ref_sel, w.name)
     mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, w.window, w.causal)
     out_e, _ = run_gpu(cpa, inp, ck, cv, w.P, mask=mask)
-    assert torch.equal(out_e.view(torch.int16), out.view(torch.int16)), "explicit != implicit"
+    assert_close(out_e, ref, w.name + "/explicit")
+    assert_explicit_matches(out_e, out, two_tile_path(w.D, w.Hq, w.Hkv, w.C), w.name)
 
 
 @pytest.mark.parametrize("D,Hkv", [(64, 1), (128, 4), (256, 2)])
