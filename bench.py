@@ -48,9 +48,9 @@ KERNEL_SOURCES = {
 }
 MEASURED_TRAFFIC = {
     # long-context chunk call: prep + attn_pair + merge, one ncu capture of the second call
-    "prefill": {"src": "8f2d2ae8532ff6a1", "bytes": 656854784},
+    "prefill": {"src": "223d26595dc7ad1c", "bytes": 657351424},
     # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0084 x)
-    "decode": {"src": "7bf918dfe065a95a", "bytes": 4836710031},
+    "decode": {"src": "6ce102dddbe87942", "bytes": 4836242101},
 }
 
 def source_hash(kind):
