@@ -222,52 +222,89 @@ def setup_parts(cpa, dev):
 
 
 def host_mirror(parts):
-    """Pinned host copies of every per-step input and output (for the e2e number)."""
+    """Pinned host copies of every per-step input and output, and a second
+    device set of inputs and outputs, so that one step's copies overlap the
+    neighbouring steps' compute (for the e2e number)."""
     h2d = d2h = 0
     for p in parts.values():
         p.host = {k: v.cpu().pin_memory() for k, v in p.inp.items()}
-        p.host_out = torch.empty(p.out.shape, dtype=p.out.dtype, pin_memory=True)
+        p.host_out = [torch.empty(p.out.shape, dtype=p.out.dtype, pin_memory=True) for _ in range(2)]
+        p.inps = [p.inp, {k: v.clone() for k, v in p.inp.items()}]
+        p.outs = [p.out, torch.empty_like(p.out)]
         h2d += sum(v.numel() * v.element_size() for v in p.host.values())
-        d2h += p.host_out.numel() * p.host_out.element_size()
+        d2h += p.host_out[0].numel() * p.host_out[0].element_size()
     return h2d, d2h
 
 
-def run_step(cpa, parts, err, ev=None, e2e=False):
-    pf, dc, tl = parts["prefill"], parts["decode"], parts["tail"]
-    if e2e:
+def run_e2e(cpa, parts, err, steps, dev):
+    """`steps` serving steps end to end: every step's inputs copied in from
+    pinned host memory and its outputs copied back, on a copy stream, double
+    buffered so that step s+1's inputs arrive and step s-1's outputs leave
+    while step s computes.  Returns ms per step (CUDA events)."""
+    main = torch.cuda.current_stream(dev)
+    cs = torch.cuda.Stream(dev)
+    h_ev = [torch.cuda.Event() for _ in range(2)]
+    c_ev = [torch.cuda.Event() for _ in range(2)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def h2d(slot):
         for p in parts.values():
             for k, v in p.host.items():
-                p.inp[k].copy_(v, non_blocking=True)
+                p.inps[slot][k].copy_(v, non_blocking=True)
+        h_ev[slot].record(cs)
+
+    e0.record(main)
+    cs.wait_stream(main)
+    with torch.cuda.stream(cs):
+        for s in range(min(2, steps)):
+            h2d(s)
+    for s in range(steps):
+        slot = s % 2
+        main.wait_event(h_ev[slot])
+        run_step(cpa, parts, err, slot=slot)
+        c_ev[slot].record(main)
+        with torch.cuda.stream(cs):
+            cs.wait_event(c_ev[slot])
+            for p in parts.values():
+                p.host_out[slot].copy_(p.outs[slot], non_blocking=True)
+            if s + 2 < steps:
+                h2d(slot)
+    main.wait_stream(cs)
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
+def run_step(cpa, parts, err, ev=None, slot=0):
+    pf, dc, tl = parts["prefill"], parts["decode"], parts["tail"]
     # prefill chunk
-    i = pf.inp
+    i = pf.inps[slot] if slot else pf.inp
     pf.cache.len.copy_(pf.len0)
     if ev is not None:
         ev[0].record()
     cpa.chunk_prefill_attn(i["q"], i["k"], i["v"], i["cos"], i["sin"], pf.cache, pf.w.P, past_len=i["past_len"],
-                           n_real=i["n_real"], out=pf.out, workspace=pf.ws, err=err)
+                           n_real=i["n_real"], out=pf.outs[slot] if slot else pf.out, workspace=pf.ws, err=err)
     if ev is not None:
         ev[1].record()
     cpa.kv_append(pf.cache, i["k"], i["v"], i["cos"], i["sin"], i["n_real"], err=err)
     # decode batch
-    i = dc.inp
+    i = dc.inps[slot] if slot else dc.inp
     dc.cache.len.copy_(dc.len0)
     if ev is not None:
         ev[2].record()
     cpa.decode_step(i["q"], i["k"], i["v"], i["cos"], i["sin"], dc.cache, dc.w.P, past_len=i["past_len"],
-                    n_real=i["n_real"], out=dc.out, workspace=dc.ws, err=err)
+                    n_real=i["n_real"], out=dc.outs[slot] if slot else dc.out, workspace=dc.ws, err=err)
     if ev is not None:
         ev[3].record()
     cpa.kv_append(dc.cache, i["k"], i["v"], i["cos"], i["sin"], i["n_real"], err=err)
     # sliding-window padded tail
-    i = tl.inp
+    i = tl.inps[slot] if slot else tl.inp
     cpa.kv_snapshot_padded_append(tl.cache, i["n_real"], tl.w.C, tl.scratch, err=err)
     cpa.chunk_prefill_attn(i["q"], i["k"], i["v"], i["cos"], i["sin"], tl.cache, tl.w.P, past_len=tl.cache.len,
-                           n_real=i["n_real"], window=512, out=tl.out, workspace=tl.ws, err=err)
+                           n_real=i["n_real"], window=512, out=tl.outs[slot] if slot else tl.out, workspace=tl.ws,
+                           err=err)
     cpa.kv_append(tl.cache, i["k"], i["v"], i["cos"], i["sin"], tl.full, scratch=tl.scratch, err=err)
     cpa.kv_rollback_padded_append(tl.cache, tl.w.C, tl.scratch, err=err)
-    if e2e:
-        for p in parts.values():
-            p.host_out.copy_(p.out, non_blocking=True)
 
 
 def ours(args, rank, world, dev):
@@ -311,17 +348,10 @@ def ours(args, rank, world, dev):
     t_pf = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(K))
     t_dc = statistics.mean(evs[k][2].elapsed_time(evs[k][3]) for k in range(K))
     # end to end: host buffers in, outputs back, through the same public calls
-    for _ in range(2):
-        run_step(cpa, parts, err, e2e=True)
+    run_e2e(cpa, parts, err, 3, dev)
     barrier()
-    K2 = max(3, K // 2)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K2):
-        run_step(cpa, parts, err, e2e=True)
-    e1.record()
+    ms_e2e = run_e2e(cpa, parts, err, max(3, K // 2), dev)
     barrier()
-    ms_e2e = e0.elapsed_time(e1) / K2
     torch.cuda.synchronize()
     if int(err[0]) != 0:
         raise RuntimeError(f"device error bits {int(err[0])}")
