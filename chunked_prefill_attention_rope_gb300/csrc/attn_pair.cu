@@ -469,24 +469,32 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       auto k_ready = [&](const TilePlan&, int, int gg) -> bool {
         return mbar_wait(&bars->k_full[gg % NS], (gg / NS) & 1, abort);
       };
+      // Descriptors are formed once; the MMAs of a group step through them by
+      // constant offsets (the start-address field is address / 16), so the
+      // issuing thread spends as few instructions as possible between MMAs.
+      const uint64_t qd0 = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
       auto issue_qk = [&](int i, int gg) {
-        const uint32_t k_addr = smem_u32(sK + (gg % NS) * CF::kKBytes);
-        const uint32_t qa = q_addr + i * CF::kQBytes;
+        const uint64_t qd = qd0 + static_cast<uint64_t>(i * (CF::kQBytes >> 4));
+        const uint64_t kd = kd0 + static_cast<uint64_t>((gg % NS) * (CF::kKBytes >> 4));
+        const uint32_t d_tm = tmem + i * kBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(qa + (kk / 4) * (128 * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_addr + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024);
-          mma_bf16_ss(tmem + i * kBN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t qo = ((kk / 4) * (128 * 128) + (kk % 4) * 32) >> 4;
+          const uint32_t ko = ((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4;
+          mma_bf16_ss(d_tm, qd + qo, kd + ko, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full[i]);
       };
       auto issue_pv = [&](int i, int gg, bool first) {
-        const uint32_t v_addr = smem_u32(sV + (gg % NS) * CF::kVBytes);
+        const uint64_t vd = vd0 + static_cast<uint64_t>((gg % NS) * (CF::kVBytes >> 4));
+        const uint32_t d_tm = tmem + CF::kOCol + i * D;
+        const uint32_t p_tm = tmem + i * kBN;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kBN * 128, 1024);
-          mma_bf16_ts(tmem + CF::kOCol + i * D, tmem + i * kBN + kk * 8, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(d_tm, p_tm + kk * 8, vd + static_cast<uint32_t>((kk * 2048) >> 4), idesc_pv,
+                      (!first || kk > 0) ? 1u : 0u);
       };
       int unit, a, e;
       Block bx;
