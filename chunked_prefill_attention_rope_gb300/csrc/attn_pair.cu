@@ -70,10 +70,11 @@ struct PairCfg {
   static constexpr int kBars = kV + kStages * kVBytes;
   static constexpr int kOCol = 2 * kBN;  // O0 at [256, 256 + D), O1 at [256 + D, 256 + 2D)
   static_assert(kOCol + 2 * D <= 512, "TMEM columns");
-  // explicit mask only: a 32-row x 32-key fp32 staging tile per softmax warp,
-  // then each warp's 32 mask-row indices
-  static constexpr int kMaskStage = kBars + 256;
-  static constexpr int kMaskRows = kMaskStage + 8 * 32 * 32 * 4;
+  // a 4 KB staging tile per softmax warp (32 rows x 32 fp32 columns): the
+  // epilogue's coalesced stores and, with an explicit mask, the mask's
+  // coalesced loads; then (explicit mask only) each warp's 32 mask-row indices
+  static constexpr int kStage = kBars + 256;
+  static constexpr int kMaskRows = kStage + 8 * 32 * 32 * 4;
   static constexpr int kMaskEnd = kMaskRows + 8 * 32 * 4;
 };
 
@@ -88,7 +89,7 @@ struct __align__(8) PairBars {
 template <int D, bool EXPLICIT>
 constexpr int pair_smem_bytes() {
   static_assert(sizeof(PairBars) <= 256, "barrier block");
-  return (EXPLICIT ? PairCfg<D>::kMaskEnd : PairCfg<D>::kBars + static_cast<int>(sizeof(PairBars))) + 1024;
+  return (EXPLICIT ? PairCfg<D>::kMaskEnd : PairCfg<D>::kMaskRows) + 1024;
 }
 static_assert(pair_smem_bytes<128, true>() <= 227 * 1024, "shared memory");
 
@@ -574,8 +575,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t s_col = tmem + lanes + qi * kBN;
     const uint32_t o_col = tmem + lanes + CF::kOCol + qi * D;
     const float sl2 = p.sl2;
-    // explicit mask staging (only allocated for the explicit instantiation)
-    float4* mstage = reinterpret_cast<float4*>(smem + CF::kMaskStage) + warp * 32 * 8;
+    float4* mstage = reinterpret_cast<float4*>(smem + CF::kStage) + warp * 32 * 8;  // this warp's staging tile
     int* mrows = reinterpret_cast<int*>(smem + CF::kMaskRows) + warp * 32;
     int g = 0, seg = 0;
     bool ok = true;
@@ -801,6 +801,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int which = seg == 0 ? 0 : 1;
       const size_t slot = (static_cast<size_t>(cta) * 2 + which) * kUnitRows + qi * 128 + row;
       if (!whole && qi == 0 && row == 0) p.ptag[2 * cta + which] = unit;
+      // Each 32-column chunk of the warp's 32 rows goes through the staging
+      // tile (16-byte slots XOR-swizzled by row, conflict-free both ways) so
+      // that the global stores are row-contiguous runs: 128 bytes per row for
+      // the fp32 partial rows (consecutive slots), 64 bytes per row for the
+      // bf16 output.
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o32[32];
@@ -809,24 +814,39 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         float o[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) o[q] = empty ? 0.f : __uint_as_float(o32[q]) * inv_l;
-        if (!valid) continue;
+        __syncwarp();
         if (!whole) {
-          float* dst = p.part_o + slot * D + 32 * c;
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
-            *reinterpret_cast<float4*>(dst + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
-        } else {
-          uint16_t* dst = p.out + orow * D + 32 * c;
+          for (int k = 0; k < 8; ++k)
+            mstage[lane * 8 + (k ^ (lane & 7))] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          __syncwarp();
+          float* base = p.part_o + (slot - lane) * D + 32 * c;  // the warp's first row
 #pragma unroll
-          for (int q = 0; q < 32; q += 8) {
-            uint4 wv;
-            wv.x = pack_bf16x2(o[q + 0], o[q + 1]);
-            wv.y = pack_bf16x2(o[q + 2], o[q + 3]);
-            wv.z = pack_bf16x2(o[q + 4], o[q + 5]);
-            wv.w = pack_bf16x2(o[q + 6], o[q + 7]);
-            *reinterpret_cast<uint4*>(dst + q) = wv;
+          for (int j = 0; j < 8; ++j) {
+            const int rr = 4 * j + (lane >> 3), k = lane & 7;
+            *reinterpret_cast<float4*>(base + rr * D + 4 * k) = mstage[rr * 8 + (k ^ (rr & 7))];
           }
-          if (p.out_sel && i == sel) {
+        } else {
+          uint4* st4 = reinterpret_cast<uint4*>(mstage);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 wv;
+            wv.x = pack_bf16x2(o[8 * k + 0], o[8 * k + 1]);
+            wv.y = pack_bf16x2(o[8 * k + 2], o[8 * k + 3]);
+            wv.z = pack_bf16x2(o[8 * k + 4], o[8 * k + 5]);
+            wv.w = pack_bf16x2(o[8 * k + 6], o[8 * k + 7]);
+            st4[lane * 4 + (k ^ ((lane >> 1) & 3))] = wv;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rr = 8 * j + (lane >> 2), k = lane & 3;
+            const bool ok_r = __shfl_sync(0xffffffffu, valid, rr);
+            const unsigned long long orr = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(orow), rr);
+            const uint4 wv = st4[rr * 4 + (k ^ ((rr >> 1) & 3))];
+            if (ok_r) *reinterpret_cast<uint4*>(p.out + orr * D + 32 * c + 8 * k) = wv;
+          }
+          if (p.out_sel && valid && i == sel) {
             float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h) * D + 32 * c;
 #pragma unroll
             for (int q = 0; q < 32; q += 4)
