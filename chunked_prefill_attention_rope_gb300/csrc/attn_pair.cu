@@ -55,8 +55,9 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsAux = 96;
 constexpr int kUnitRows = 256;
 // A unit switch (Q reload, epilogue, pipeline refill) costs about this many key
-// tiles; the stream-K split charges it to every non-empty unit.
-constexpr int kSwitchCost = 2;
+// tiles (per-CTA cycle counts fitted over key tiles and segments: ~3); the
+// stream-K split charges it to every non-empty unit.
+constexpr int kSwitchCost = 3;
 
 template <int D>
 struct PairCfg {
@@ -232,7 +233,7 @@ __device__ void plan_units(const AttnParams& p) {
   if (threadIdx.x == 0) p.ustart[p.blocks] = carry;
 }
 
-// The last CTA plans (plan_units); the others rotate the chunk's queries and
+// CTA 0 plans (plan_units); the others rotate the chunk's queries and
 // keys into the workspace.  An item is one (sequence, chunk row, chunk pair)
 // and up to four heads of the combined list [query heads, key heads]: the
 // table values of its row are loaded once and the four heads' loads are
@@ -240,7 +241,7 @@ __device__ void plan_units(const AttnParams& p) {
 // every load and store is a contiguous 512-byte run per head.
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams p) {
   grid_launch_dependents();
-  if (blockIdx.x == gridDim.x - 1) {
+  if (blockIdx.x == 0) {  // the first CTA to start plans, alongside the rotations
     plan_units(p);
     return;
   }
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
   const int groups = (HH + kPrepHeads - 1) / kPrepHeads;
   const long long total = static_cast<long long>(p.B) * groups * p.C * HP;
   const long long stride = static_cast<long long>(gridDim.x - 1) * blockDim.x;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total; it += stride) {
+  for (long long it = (blockIdx.x - 1) * static_cast<long long>(blockDim.x) + threadIdx.x; it < total; it += stride) {
     const int kc = static_cast<int>(it % HP);
     long long t = it / HP;
     const int i = static_cast<int>(t % p.C);
@@ -820,11 +821,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           for (int k = 0; k < 8; ++k)
             mstage[lane * 8 + (k ^ (lane & 7))] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
           __syncwarp();
+          // partial rows stay in L2 for merge_units_kernel while the K/V stream passes
           float* base = p.part_o + (slot - lane) * D + 32 * c;  // the warp's first row
+          const uint64_t keep = l2_policy_keep();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int rr = 4 * j + (lane >> 3), k = lane & 7;
-            *reinterpret_cast<float4*>(base + rr * D + 4 * k) = mstage[rr * 8 + (k ^ (rr & 7))];
+            st_global_hint(reinterpret_cast<float4*>(base + rr * D + 4 * k), mstage[rr * 8 + (k ^ (rr & 7))], keep);
           }
         } else {
           uint4* st4 = reinterpret_cast<uint4*>(mstage);
@@ -928,6 +931,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnPa
   if (np < 0) return;
   const int n_real = p.n_real ? min(max(p.n_real[x.b], 0), p.C) : p.C;
   const int sel = p.sel_row ? p.sel_row[x.b] : n_real - 1;
+  const uint64_t drop = l2_policy_drop();
   constexpr int kRowsPerWarp = kMergeRows / (kMergeThreads / 32);
   for (int j0 = 0; j0 < kRowsPerWarp; j0 += kMergeRowBatch) {
     int r[kMergeRowBatch], i[kMergeRowBatch], h[kMergeRowBatch];
@@ -960,7 +964,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnPa
           if (live[u] && k0 + k < np) {
             const size_t sidx = static_cast<size_t>(piece_slot[k0 + k]) * kUnitRows + r[u];
             ls[u][k] = p.part_lse[sidx];
-            o[u][k] = *reinterpret_cast<const Vec*>(p.part_o + sidx * D + lane * V);
+            if constexpr (V == 4)  // the last read of these rows: let L2 drop them first
+              o[u][k] = ld_global_hint(reinterpret_cast<const float4*>(p.part_o + sidx * D + lane * V), drop);
+            else
+              o[u][k] = *reinterpret_cast<const Vec*>(p.part_o + sidx * D + lane * V);
           }
         }
 #pragma unroll
