@@ -765,21 +765,29 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             emit(pv, c);
           }
         } else {
-          // P = 2^(t - m) from the t written above
+          // P = 2^(t - m) from the t written above, two chunks per
+          // tensor-memory round trip (chunk c + 1's P lands over chunk c's t,
+          // already in registers)
           const float nm = live ? -m_run : -INFINITY;
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(s_col + 32 * c, r);
-            tmem_ld_wait(r);
-            float pv[32];
+          for (int c = 0; c < kBN / 32; c += 2) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(s_col + 32 * c, ra);
+            tmem_ld32(s_col + 32 * (c + 1), rb);
+            tmem_ld_wait(ra);
+            tmem_ld_wait(rb);
 #pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const float2 y = fadd2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), make_float2(nm, nm));
-              pv[q] = fast_exp2(y.x);
-              pv[q + 1] = fast_exp2(y.y);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t (&r)[32] = h ? rb : ra;
+              float pv[32];
+#pragma unroll
+              for (int q = 0; q < 32; q += 2) {
+                const float2 y = fadd2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), make_float2(nm, nm));
+                pv[q] = fast_exp2(y.x);
+                pv[q + 1] = fast_exp2(y.y);
+              }
+              emit(pv, c + h);
             }
-            emit(pv, c);
           }
         }
         const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
