@@ -207,17 +207,26 @@ def test_page1_shape_eighteen_layers_explicit_masks():
         assert torch.equal(out_i.view(torch.int16), out.view(torch.int16)), f"page1/L{layer} implicit"
 
 
-def sample_check(cpa, w, pairs, device_gen=False):
-    """Run the full workload on the GPU, check sampled (b, kv-head) groups on the oracle."""
+def sample_check(cpa, w, pairs, device_gen=False, explicit=False):
+    """Run the full workload on the GPU, check sampled (b, kv-head) groups on the
+    oracle.  `explicit`: pass the mask as an explicit [B, Hq, C, P+C] tensor,
+    each sequence's rows built by the oracle's mask function and repeated over
+    the heads on the device."""
     dev = DEV if device_gen else "cpu"
     inp = make_chunk_inputs(w, device=dev)
     ck, cv = make_cache(w, device=dev)
     d = lambda t: t.to(DEV)
+    mask = None
+    if explicit:
+        rows = [torch.from_numpy(O.explicit_mask(int(inp["past_len"][b]), int(inp["n_real"][b]), w.C, w.P,
+                                                 w.window, w.causal).astype(np.float32)) for b in range(w.B)]
+        mask = torch.stack(rows).to(DEV)[:, None].expand(w.B, w.Hq, w.C, w.P + w.C).contiguous()
     cache = cpa.KVCache(d(ck), d(cv), d(inp["past_len"]).clone())
     err = cpa.new_error_word()
     out, sel = cpa.chunk_prefill_attn(d(inp["q"]), d(inp["k"]), d(inp["v"]), d(inp["cos"]), d(inp["sin"]),
                                       cache, w.P, past_len=d(inp["past_len"]), n_real=d(inp["n_real"]),
-                                      causal=bool(w.causal), want_sel=True, err=err)
+                                      causal=bool(w.causal), mask=mask, want_sel=True, err=err)
+    del mask
     torch.cuda.synchronize()
     assert int(err[0]) == 0
     G = w.Hq // w.Hkv
@@ -241,6 +250,17 @@ def test_packed_batch_full_size_sampled():
     order = np.argsort(L.numpy())
     pairs = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
     sample_check(cpa, w, pairs)
+
+
+def test_packed_batch_full_size_explicit_mask_sampled():
+    """The packed batch with its 1.1 GB explicit fp32 mask, in the launch
+    configuration the bench times."""
+    cpa = lib()
+    w = WORKLOADS["packed_batch"]
+    L = w.past_lens()
+    order = np.argsort(L.numpy())
+    pairs = [(int(order[0]), 1), (int(order[-1]), 6), (int(order[len(order) // 2]), 4)]
+    sample_check(cpa, w, pairs, device_gen=True, explicit=True)
 
 
 def test_long_context_full_size_sampled():
