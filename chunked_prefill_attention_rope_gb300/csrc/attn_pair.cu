@@ -887,16 +887,18 @@ constexpr int kMaxCtas = 256;
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRows = 64;  // rows of one unit per merge block
 constexpr int kMergeRowBatch = 2;
-constexpr int kMergePieceBatch = 4;
+constexpr int kMergePieceBatch = 2;
 
 // One block per (unit, 64-row slab).  Warp 0 finds the unit's pieces (the
 // partial-result slots tagged with the unit, in CTA order) with one load per
-// lane; then each warp merges 8 rows, two rows and four pieces per batch with
+// lane; then each warp merges 8 rows, two rows and two pieces per batch with
 // all their loads issued before any use.  Pieces combine in CTA order with a
 // running maximum (one batch, and so the plain max-shifted weighted sum, when
-// a unit has at most four pieces).
+// a unit has two pieces, the usual case).  Registers are capped at 64 so that
+// four blocks fit an SM: the grid then runs in under two waves (at 90
+// registers it took 3.4).
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_units_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const AttnParams p) {
   __shared__ int piece_slot[kMaxCtas];  // partial-result slot of each piece, in CTA order
   __shared__ int n_pieces;
   constexpr int V = D / 32;  // floats per lane
