@@ -695,8 +695,11 @@ __global__ void combine_kernel(const AttnParams p) {
   const int b = bh / p.Hq;
   const int h = bh % p.Hq;
   const size_t stride = static_cast<size_t>(rows);
+  // the splits' log2-sum-exps spread over the lanes, then the warp's maximum
   float lmax = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) lmax = fmaxf(lmax, p.part_lse[s * stride + row]);
+  for (int s = lane; s < p.splits; s += 32) lmax = fmaxf(lmax, p.part_lse[s * stride + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
   const int D = p.D;
   const int per = D / 32;  // 2, 4 or 8 values per lane
   float acc[8];
@@ -704,15 +707,36 @@ __global__ void combine_kernel(const AttnParams p) {
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (lmax != -INFINITY) {
-    for (int s = 0; s < p.splits; ++s) {
-      const float ls = p.part_lse[s * stride + row];
-      if (ls == -INFINITY) continue;
-      const float w = fast_exp2(ls - lmax);
-      wsum += w;
-      const float* src = p.part_o + (s * stride + row) * D + lane * per;
+    // splits in order, four at a time with their loads issued before use
+    constexpr int kB = 4;
+    for (int s0 = 0; s0 < p.splits; s0 += kB) {
+      float ls[kB], o[kB][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (e < per) acc[e] = __fmaf_rn(w, src[e], acc[e]);
+      for (int k = 0; k < kB; ++k) {
+        ls[k] = -INFINITY;
+        if (s0 + k < p.splits) {
+          const size_t sr = (s0 + k) * stride + row;
+          ls[k] = p.part_lse[sr];
+          const float* src = p.part_o + sr * D + lane * per;
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            if (e < per) {
+              const float2 v = *reinterpret_cast<const float2*>(src + e);
+              o[k][e] = v.x;
+              o[k][e + 1] = v.y;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        if (ls[k] == -INFINITY) continue;
+        const float w = fast_exp2(ls[k] - lmax);
+        wsum += w;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e < per) acc[e] = __fmaf_rn(w, o[k][e], acc[e]);
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
