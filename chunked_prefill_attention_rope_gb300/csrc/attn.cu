@@ -645,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // grid start at once.
 __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
   grid_launch_dependents();
+  grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
   const int D = p.D;
   const int HP = D / 16;
   const long long total = static_cast<long long>(p.B) * p.Hkv * p.C * HP;
@@ -771,8 +772,7 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
   const long long items = static_cast<long long>(p.B) * p.Hkv * p.C * (D / 16);
   const int kblocks = static_cast<int>(max(1LL, min(static_cast<long long>(152) * 8, (items + 255) / 256)));
-  rope_chunk_k_kernel<<<kblocks, 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(rope_chunk_k_kernel, dim3(kblocks), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

@@ -241,6 +241,7 @@ __device__ void plan_units(const AttnParams& p) {
 // every load and store is a contiguous 512-byte run per head.
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams p) {
   grid_launch_dependents();
+  grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
   if (blockIdx.x == 0) {  // the first CTA to start plans, alongside the rotations
     plan_units(p);
     return;
@@ -1067,8 +1068,7 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
                           (p.D / 16);
   const int rope_blocks =
       static_cast<int>(max(1LL, min(static_cast<long long>(65535) * 4, (items + kPrepThreads - 1) / kPrepThreads)));
-  prep_kernel<<<rope_blocks + 1, kPrepThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(prep_kernel, dim3(rope_blocks + 1), dim3(kPrepThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_dependent(kern, dim3(p.ctas), dim3(kThreadsPair), smem, stream, maps[0], maps[1], maps[2], maps[3],
                        maps[4], p);

@@ -64,6 +64,8 @@ __device__ __forceinline__ int clamp_rows(int n, int C, int32_t* err, bool repor
 // ---------------------------------------------------------------- global append
 
 __global__ void global_append_rows(CacheView c, ChunkView x, int B, int Hkv, int D, int C, int32_t* err) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int HP = D / 16;
   const long long total = static_cast<long long>(B) * Hkv * C * HP;
   for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
@@ -87,6 +89,8 @@ __global__ void global_append_rows(CacheView c, ChunkView x, int B, int Hkv, int
 }
 
 __global__ void global_append_len(CacheView c, const int32_t* n_rows, int B, int C) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int n = min(max(n_rows[b], 0), C);
@@ -100,6 +104,8 @@ __global__ void global_append_len(CacheView c, const int32_t* n_rows, int B, int
 // eviction ([S + e, L)) into staging.
 __global__ void sliding_stage(CacheView c, const int32_t* n_rows, int B, int Hkv, int D, int C,
                               Hdr* hdr, uint16_t* stage_k, uint16_t* stage_v, int32_t* err) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
   const long long total = static_cast<long long>(B) * Hkv * W * CH;
@@ -136,6 +142,8 @@ __global__ void sliding_stage(CacheView c, const int32_t* n_rows, int B, int Hkv
 // [L - e, L - e + n), then len = L - e + n.
 __global__ void sliding_commit(CacheView c, ChunkView x, int B, int Hkv, int D, int C, const Hdr* hdr,
                                const uint16_t* stage_k, const uint16_t* stage_v) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int HP = D / 16;
   const int rows = W + C;
@@ -174,6 +182,8 @@ __global__ void sliding_commit(CacheView c, ChunkView x, int B, int Hkv, int D, 
 // beyond an exact append of n rows.
 __global__ void snapshot_kernel(CacheView c, const int32_t* n_real, int B, int Hkv, int D, int C, Hdr* hdr,
                                 uint16_t* saved_k, uint16_t* saved_v, int32_t* err) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
   const long long total = static_cast<long long>(B) * Hkv * C * CH;
@@ -212,6 +222,8 @@ __global__ void snapshot_kernel(CacheView c, const int32_t* n_real, int B, int H
 // rows [S, keep) that must move right by d = e_pad - e_ex.
 __global__ void rollback_stage(CacheView c, int B, int Hkv, int D, int C, const Hdr* snap, Hdr* roll,
                                uint16_t* stage_k, uint16_t* stage_v, int32_t* err) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
   const long long total = static_cast<long long>(B) * Hkv * W * CH;
@@ -248,6 +260,8 @@ __global__ void rollback_stage(CacheView c, int B, int Hkv, int D, int C, const 
 __global__ void rollback_commit(CacheView c, int B, int Hkv, int D, int C, Hdr* snap, const Hdr* roll,
                                 const uint16_t* stage_k, const uint16_t* stage_v, const uint16_t* saved_k,
                                 const uint16_t* saved_v) {
+  grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
+  grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
   const int rows = W + C;
@@ -315,9 +329,9 @@ SlidingScratch sliding_scratch_layout(int B, int Hkv, int D, int C, int W) {
 cudaError_t launch_global_append(const CacheView& c, const ChunkView& x, int B, int Hkv, int D, int C,
                                  int32_t* err, cudaStream_t s) {
   const long long items = static_cast<long long>(B) * Hkv * C * (D / 16);
-  global_append_rows<<<grid_for(items), kThreads, 0, s>>>(c, x, B, Hkv, D, C, err);
-  global_append_len<<<(B + 127) / 128, 128, 0, s>>>(c, x.n_rows, B, C);
-  return cudaGetLastError();
+  cudaError_t e = launch_dependent(global_append_rows, grid_for(items), dim3(kThreads), 0, s, c, x, B, Hkv, D, C, err);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(global_append_len, dim3((B + 127) / 128), dim3(128), 0, s, c, x.n_rows, B, C);
 }
 
 cudaError_t launch_sliding_append(const CacheView& c, const ChunkView& x, int B, int Hkv, int D, int C,
@@ -327,20 +341,22 @@ cudaError_t launch_sliding_append(const CacheView& c, const ChunkView& x, int B,
   uint16_t* sk = reinterpret_cast<uint16_t*>(scratch + L.stage_k);
   uint16_t* sv = reinterpret_cast<uint16_t*>(scratch + L.stage_v);
   const long long items1 = static_cast<long long>(B) * Hkv * c.window * (D / 8);
-  sliding_stage<<<grid_for(items1), kThreads, 0, s>>>(c, x.n_rows, B, Hkv, D, C, hdr, sk, sv, err);
+  cudaError_t e = launch_dependent(sliding_stage, grid_for(items1), dim3(kThreads), 0, s, c, x.n_rows, B, Hkv, D, C,
+                                   hdr, sk, sv, err);
+  if (e != cudaSuccess) return e;
   const long long items2 = static_cast<long long>(B) * Hkv * (c.window + C) * (D / 16);
-  sliding_commit<<<grid_for(items2), kThreads, 0, s>>>(c, x, B, Hkv, D, C, hdr, sk, sv);
-  return cudaGetLastError();
+  return launch_dependent(sliding_commit, grid_for(items2), dim3(kThreads), 0, s, c, x, B, Hkv, D, C,
+                          static_cast<const Hdr*>(hdr), static_cast<const uint16_t*>(sk),
+                          static_cast<const uint16_t*>(sv));
 }
 
 cudaError_t launch_snapshot(const CacheView& c, const int32_t* n_real, int B, int Hkv, int D, int C,
                             uint8_t* scratch, int32_t* err, cudaStream_t s) {
   const SlidingScratch L = sliding_scratch_layout(B, Hkv, D, C, c.window);
   const long long items = static_cast<long long>(B) * Hkv * C * (D / 8);
-  snapshot_kernel<<<grid_for(items), kThreads, 0, s>>>(
-      c, n_real, B, Hkv, D, C, reinterpret_cast<Hdr*>(scratch + L.hdr_snap),
-      reinterpret_cast<uint16_t*>(scratch + L.saved_k), reinterpret_cast<uint16_t*>(scratch + L.saved_v), err);
-  return cudaGetLastError();
+  return launch_dependent(snapshot_kernel, grid_for(items), dim3(kThreads), 0, s, c, n_real, B, Hkv, D, C,
+                          reinterpret_cast<Hdr*>(scratch + L.hdr_snap), reinterpret_cast<uint16_t*>(scratch + L.saved_k),
+                          reinterpret_cast<uint16_t*>(scratch + L.saved_v), err);
 }
 
 cudaError_t launch_rollback(const CacheView& c, int B, int Hkv, int D, int C, uint8_t* scratch, int32_t* err,
@@ -351,12 +367,14 @@ cudaError_t launch_rollback(const CacheView& c, int B, int Hkv, int D, int C, ui
   uint16_t* sk = reinterpret_cast<uint16_t*>(scratch + L.stage_k);
   uint16_t* sv = reinterpret_cast<uint16_t*>(scratch + L.stage_v);
   const long long items1 = static_cast<long long>(B) * Hkv * c.window * (D / 8);
-  rollback_stage<<<grid_for(items1), kThreads, 0, s>>>(c, B, Hkv, D, C, snap, roll, sk, sv, err);
+  cudaError_t e = launch_dependent(rollback_stage, grid_for(items1), dim3(kThreads), 0, s, c, B, Hkv, D, C,
+                                   static_cast<const Hdr*>(snap), roll, sk, sv, err);
+  if (e != cudaSuccess) return e;
   const long long items2 = static_cast<long long>(B) * Hkv * (c.window + C) * (D / 8);
-  rollback_commit<<<grid_for(items2), kThreads, 0, s>>>(c, B, Hkv, D, C, snap, roll, sk, sv,
-                                                        reinterpret_cast<uint16_t*>(scratch + L.saved_k),
-                                                        reinterpret_cast<uint16_t*>(scratch + L.saved_v));
-  return cudaGetLastError();
+  return launch_dependent(rollback_commit, grid_for(items2), dim3(kThreads), 0, s, c, B, Hkv, D, C, snap,
+                          static_cast<const Hdr*>(roll), static_cast<const uint16_t*>(sk),
+                          static_cast<const uint16_t*>(sv), reinterpret_cast<const uint16_t*>(scratch + L.saved_k),
+                          reinterpret_cast<const uint16_t*>(scratch + L.saved_v));
 }
 
 }  // namespace cpa

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
   using CF = DecCfg<D>;
   constexpr int NS = CF::kStages;
   grid_launch_dependents();  // combine_kernel may be scheduled now; it waits for this grid
+  grid_dependency_wait();    // launched as a dependent: whatever the launches before it wrote
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NB = D / 8;   // n-blocks of O
   extern __shared__ uint8_t smem_raw[];
@@ -431,8 +432,7 @@ static cudaError_t launch_decode_t(const CUtensorMap* maps, const AttnParams& p,
     attr_set = true;
   }
   dim3 grid(p.splits, p.Hkv, p.B);
-  kern<<<grid, kDThreads, CF::kSmem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(kDThreads), CF::kSmem, stream, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 template <int D>
