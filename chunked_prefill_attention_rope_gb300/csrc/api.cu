@@ -67,8 +67,9 @@ struct Geometry {
 //          at most, balanced on the device by stream-K (no split-KV).
 //   decode (C = 1) and single-tile chunks: split-KV, each split owning a fixed
 //          range of the key-tile index space (see tiles.cuh); splits grow while
-//          the grid is under two waves, and decode caps a CTA at about 16 key
-//          tiles of the longest possible past.
+//          the grid is under two waves, and one-query-tile calls cap a CTA at
+//          about 32 (decode kernel) or 16 (single-tile kernel) key tiles of the
+//          longest possible past.
 Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   Geometry g;
   g.G = Hq / Hkv;
@@ -89,7 +90,11 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
   const long long ctas = static_cast<long long>(B) * Hkv * g.nq;
   int s = 1;
   while (ctas * s < 2LL * sms && s * 2 <= max_tiles) s *= 2;
-  if (g.nq == 1 && max_tiles > 32) s = max(s, (max_tiles + 15) / 16);
+  // one query tile per (sequence, kv head): enough splits that a CTA sees at
+  // most ~32 key tiles of the longest past on the decode kernel (measured
+  // best of 8/16/32/64/128 on a 64-sequence batch), ~16 on the single-tile one
+  const int per_cta = g.path == kPathDecode ? 32 : 16;
+  if (g.nq == 1 && max_tiles > 32) s = max(s, (max_tiles + per_cta - 1) / per_cta);
   g.splits = max(1, min(s, max(1, max_tiles)));
   g.cluster = g.path == kPathSingle && (g.splits == 2 || g.splits == 4 || g.splits == 8) &&
               attn_cluster_ok(D, g.splits);

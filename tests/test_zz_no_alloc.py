@@ -52,7 +52,7 @@ def test_noalloc_matches_regular_entry_point_two_calls_in_a_row():
 
 def test_noalloc_refuses_problems_beyond_its_array():
     cpa = lib()
-    B, Hq, Hkv, D, P = 64, 32, 8, 128, 32768
+    B, Hq, Hkv, D, P = 128, 32, 8, 128, 32768   # a decode batch whose split-KV partials need ~18 MiB
     assert cpa.attn_workspace_size(B, Hq, Hkv, D, 1, P) > 16 << 20
     q = torch.zeros((B, Hq, 1, D), dtype=torch.bfloat16, device=DEV)
     kv = torch.zeros((B, Hkv, 1, D), dtype=torch.bfloat16, device=DEV)
