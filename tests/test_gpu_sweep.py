@@ -75,3 +75,20 @@ def test_sweep_matches_oracle(w):
     out_e, _, _ = run(cpa, inp, ck, cv, w, mask=mask)
     assert_close(out_e, ref, w.name + "/explicit")
     assert_explicit_matches(out_e, out, two_tile_path(w.D, w.Hq, w.Hkv, w.C), w.name)
+
+
+@pytest.mark.parametrize("w", CASES[::3], ids=lambda w: w.name)
+def test_sweep_fp16_cache_matches_oracle(w):
+    """Every third drawn shape over an fp16 KV cache (the bf16 N(0,1) cache
+    values convert exactly), against the oracle's fp16 reading: products in
+    fp16, P rounded to half ("Pad the chunked-prefill tail for sliding-window
+    models", Declined with rationale: the fp16 KV-cache runtime option)."""
+    cpa = lib()
+    inp = make_chunk_inputs(w)
+    ck, cv = (t.to(torch.float16) for t in make_cache(w))
+    out, out_sel, sel = run(cpa, inp, ck, cv, w)
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                               inp["past_len"], inp["n_real"], w.window, w.causal, sel_row=sel)
+    assert_close(out, ref, w.name + "/f16")
+    if (inp["n_real"] > 0).all():
+        check_argmax(out_sel, ref_sel, w.name + "/f16")
