@@ -92,3 +92,14 @@ def test_sweep_fp16_cache_matches_oracle(w):
     assert_close(out, ref, w.name + "/f16")
     if (inp["n_real"] > 0).all():
         check_argmax(out_sel, ref_sel, w.name + "/f16")
+
+
+@pytest.mark.parametrize("w", [w for w in CASES if w.C > 1][::2], ids=lambda w: w.name)
+def test_sweep_fused_append_equals_attention_then_append(w):
+    """cpa_chunk_prefill_attn_append on every second drawn chunk shape gives
+    exactly the bits of attention followed by cpa_kv_append: output, selected
+    row, cache bytes, lengths and error word ("functiongemma: chunk
+    prefill-with-past graph", Change: K/V extended by the chunk)."""
+    from test_gpu_fused_append import run as run_pair, same
+    cpa = lib()
+    same(run_pair(cpa, w, fused=True, alias=True), run_pair(cpa, w, fused=False, alias=False))
