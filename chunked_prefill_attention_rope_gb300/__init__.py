@@ -61,7 +61,8 @@ class _AttnArgs(ctypes.Structure):
                 ("mask", ctypes.c_void_p), ("past_len", ctypes.c_void_p), ("n_real", ctypes.c_void_p),
                 ("window", ctypes.c_int), ("causal", ctypes.c_int), ("sel_row", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("out_sel", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("err", ctypes.c_void_p)]
+                ("workspace_bytes", ctypes.c_size_t), ("err", ctypes.c_void_p),
+                ("sm_budget", ctypes.c_int)]
 
 
 _LIB = None
@@ -167,7 +168,7 @@ def cache_scratch_size(cache: KVCache, C: int) -> int:
 def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
           window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
           out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None,
-          alloc_workspace: bool = True, append_rows=None):
+          alloc_workspace: bool = True, append_rows=None, sm_budget: int = 0):
     lib = load_library()
     B, Hq, C, D = q.shape
     Hkv = k_new.shape[1]
@@ -196,7 +197,7 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
                   cos.data_ptr(), sin.data_ptr(), ctypes.pointer(cs), _ptr(mask), _ptr(past_len),
                   _ptr(n_real), int(window), 1 if causal else 0, _ptr(sel_row), out.data_ptr(),
                   _ptr(out_sel), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                  err.data_ptr())
+                  err.data_ptr(), int(sm_budget))
     if append_rows is not None:
         _need(append_rows, "n_rows", torch.int32, (B,))
         _check(getattr(lib, entry)(ctypes.byref(a), append_rows.data_ptr(), _stream(stream)))

@@ -70,14 +70,15 @@ struct Geometry {
 //          the grid is under two waves, and one-query-tile calls cap a CTA at
 //          about 32 (decode kernel) or 16 (single-tile kernel) key tiles of the
 //          longest possible past.
-Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P) {
+Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0) {
   Geometry g;
   g.G = Hq / Hkv;
   g.R = 128 / g.G;
   g.nq = (C + g.R - 1) / g.R;
   g.teams = PairTeams{};
   g.cluster = false;
-  const int sms = num_sms();
+  const int dev_sms = num_sms();
+  const int sms = sm_budget > 0 && sm_budget < dev_sms ? sm_budget : dev_sms;
   if (attn_uses_pair(D, g.nq) && !attn_uses_decode(D, C, g.G)) {
     g.path = kPathPair;
     g.splits = 1;
@@ -169,7 +170,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   if (a->Hq % a->Hkv != 0 || a->Hq / a->Hkv > 128) return CPA_ERR_SHAPE;
   if (!valid_d(a->D)) return CPA_ERR_UNSUPPORTED;
   if (decode && a->C != 1) return CPA_ERR_SHAPE;
-  if (a->window < 0) return CPA_ERR_SHAPE;
+  if (a->window < 0 || a->sm_budget < 0) return CPA_ERR_SHAPE;
   const cpa_status cs = check_cache(a->cache, a->D);
   if (cs != CPA_OK) return cs;
   if (a->P > a->cache->cap) return CPA_ERR_SHAPE;
@@ -181,7 +182,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     return CPA_ERR_ALIGN;
   if (static_cast<long long>(a->B) * a->Hq * a->C * a->D > (1LL << 40)) return CPA_ERR_SHAPE;
 
-  const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
+  const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, a->sm_budget);
   const size_t need = workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C);
   if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)))
     return CPA_ERR_WORKSPACE;
@@ -222,6 +223,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.f16 = c->dtype == CPA_KV_F16 ? 1 : 0;
   p.sink = (!a->mask && a->cache->kind == CPA_CACHE_SLIDING) ? a->cache->sink : 0;
   p.out = static_cast<uint16_t*>(a->out);
+  p.hold_dependents = a->sm_budget > 0 && a->sm_budget < num_sms() ? 1 : 0;
   p.out_sel = a->out_sel;
   p.err = a->err;
   p.k_new = static_cast<const uint16_t*>(a->k_new);

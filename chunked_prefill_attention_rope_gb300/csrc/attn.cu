@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
 
-  grid_launch_dependents();  // combine_kernel (if any) may be scheduled now; it waits for this grid
+  // combine_kernel (if any) may be scheduled now, except on a partial SM
+  // budget (then as this grid ends); it waits for this grid
+  if (!p.hold_dependents) grid_launch_dependents();
   const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
   const int my_nt = tp.count();
 

@@ -409,9 +409,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     tmem_relinquish();
   }
   __syncthreads();
-  // the merge grid may be scheduled now; this grid's inputs (plan, rotated
-  // Q and keys) come from prep_kernel, launched just before it
-  grid_launch_dependents();
+  // the merge grid may be scheduled now (on a partial SM budget only as this
+  // grid ends, leaving the other SMs to other streams); this grid's inputs
+  // (plan, rotated Q and keys) come from prep_kernel, launched just before it
+  if (!p.hold_dependents) grid_launch_dependents();
   grid_dependency_wait();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;

@@ -89,8 +89,10 @@ __global__ void __launch_bounds__(kDThreads, 2)
                        const AttnParams p) {
   using CF = DecCfg<D>;
   constexpr int NS = CF::kStages;
-  grid_launch_dependents();  // combine_kernel may be scheduled now; it waits for this grid
-  grid_dependency_wait();    // launched as a dependent: whatever the launches before it wrote
+  // combine_kernel may be scheduled now (on a partial SM budget, as this grid
+  // ends); it waits for this grid
+  if (!p.hold_dependents) grid_launch_dependents();
+  grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NB = D / 8;   // n-blocks of O
   extern __shared__ uint8_t smem_raw[];

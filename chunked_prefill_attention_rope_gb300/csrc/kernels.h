@@ -52,6 +52,7 @@ struct AttnParams {
   int blocks;       // B * Hkv * nblk
   int teams;        // teams of CTAs
   int ctas;         // persistent CTAs = teams * team
+  int hold_dependents;  // SM budget below the device: follow-up kernels launch only as the grid ends
   const uint16_t* k_new;  // chunk keys before RoPE [B, Hkv, C, D]
   uint16_t* q_rot;        // rotated queries [B, Hq, C, D] (workspace)
   uint16_t* k_rot;        // rotated chunk keys [B, Hkv, C, D] (workspace)

@@ -143,6 +143,14 @@ typedef struct {
  *          (split-KV partial results, rotated copies of the chunk's queries
  *          and keys); may be NULL when that size is 0.
  *   err    device int32 error word (required).
+ *   sm_budget  0, or the number of SMs the call may occupy: a value below
+ *          the device's SM count sizes the persistent grid for that many
+ *          SMs and keeps the call's follow-up kernels from taking SMs before
+ *          its attention grid ends, so that work issued on another stream
+ *          (for example a decode batch beside a prefill chunk, the mixed
+ *          batch of chunked prefill serving) runs on the rest.  The result
+ *          does not depend on it beyond rounding order.  Negative ->
+ *          CPA_ERR_SHAPE.
  */
 typedef struct {
   int B, Hq, Hkv, D, C, P;
@@ -164,6 +172,7 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   int32_t* err;
+  int sm_budget;
 } cpa_attn_args;
 
 /* One chunk of C rows against the cache ([P1, Change]; cost scales with C,
