@@ -250,6 +250,10 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     uint8_t* w = static_cast<uint8_t*>(a->workspace);
     const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, a->D, a->C, t);
     p.ustart = reinterpret_cast<int32_t*>(w + L.ustart);
+    p.perm = t.perm && !a->mask && p.sink <= 0 ? 1 : 0;
+    p.uorder = reinterpret_cast<int32_t*>(w + L.uorder);
+    p.upos = reinterpret_cast<int32_t*>(w + L.upos);
+    p.tlo = reinterpret_cast<int32_t*>(w + L.tlo);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
     p.part_lse = reinterpret_cast<float*>(w + L.part_lse);
     p.ptag = reinterpret_cast<int32_t*>(w + L.ptag);

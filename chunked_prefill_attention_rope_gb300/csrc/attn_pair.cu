@@ -58,6 +58,10 @@ constexpr int kUnitRows = 256;
 // tiles (per-CTA cycle counts fitted over key tiles and segments: ~3); the
 // stream-K split charges it to every non-empty unit.
 constexpr int kSwitchCost = 3;
+// A cut unit costs its second piece another switch and goes through the merge
+// kernel; a plan that deals whole blocks is kept while its busiest team has at
+// most this many key tiles more than the even split's share.
+constexpr int kCutCost = 2 * kSwitchCost;
 
 template <int D>
 struct PairCfg {
@@ -146,10 +150,15 @@ __device__ __forceinline__ int unit_at(const int32_t* start, int U, long long x)
 
 // Walks the (block, first tile, end tile) segments of a team's range of cost
 // positions, for one member: segments whose pair does not exist are skipped.
+// PERM: the blocks are walked in the planned order p.uorder and team t's
+// range is [p.tlo[t], p.tlo[t + 1]) (a whole-block deal or the even split);
+// otherwise blocks are in index order and the ranges split the costs evenly.
+template <bool PERM>
 struct SegWalk {
+  using Pos = typename std::conditional<PERM, int, long long>::type;  // tlo holds 32-bit positions
   const int32_t* start;
   int NB, g, member;
-  long long lo, hi;
+  Pos lo, hi;
   const AttnParams* pp;
   __device__ __forceinline__ void init(const AttnParams& p, int cta) {
     pp = &p;
@@ -157,9 +166,14 @@ struct SegWalk {
     NB = p.blocks;
     member = cta % p.team;
     const int t = cta / p.team;
-    const long long T = start[NB];
-    lo = cta_lo(T, t, p.teams);
-    hi = cta_lo(T, t + 1, p.teams);
+    if (PERM) {
+      lo = p.tlo[t];
+      hi = p.tlo[t + 1];
+    } else {
+      const long long T = start[NB];
+      lo = cta_lo(T, t, p.teams);
+      hi = cta_lo(T, t + 1, p.teams);
+    }
     g = lo < hi ? unit_at(start, NB, lo) : NB;
   }
   // Next segment holding at least one key tile of this member's unit; false
@@ -167,12 +181,12 @@ struct SegWalk {
   // [start[g], start[g+1]): first the switch cost, then one per key tile.
   __device__ __forceinline__ bool next(int& unit, Block& blk, int& a, int& e) {
     while (g < NB && start[g] < hi) {
-      const long long t0 = start[g] + kSwitchCost, s1 = start[g + 1];
+      const Pos t0 = start[g] + kSwitchCost, s1 = start[g + 1];
       const int cur = g++;
-      const long long aa = lo > t0 ? lo : t0;
-      const long long ee = hi < s1 ? hi : s1;
+      const Pos aa = lo > t0 ? lo : t0;
+      const Pos ee = hi < s1 ? hi : s1;
       if (ee <= aa) continue;
-      const Block x = block_of(*pp, cur);
+      const Block x = block_of(*pp, PERM ? pp->uorder[cur] : cur);
       const int pair = x.blk * pp->team + member;
       if (pair >= pp->pairs) continue;
       blk = x;
@@ -190,23 +204,29 @@ struct SegWalk {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepHeads = 4;  // heads rotated per item with one table load (two CTAs per SM)
 
-// Cost of every block (its live key tiles plus the switch cost) and the
-// exclusive prefix sum of the costs, by one CTA of kPrepThreads threads.
-__device__ void plan_units(const AttnParams& p) {
+// Blocks the whole-block plan can order (their costs sit in shared memory).
+constexpr int kPlanSortMax = 1024;
+
+// Key tiles of block u plus the switch cost (0 for a block without live tiles).
+__device__ __forceinline__ int block_cost(const AttnParams& p, int u) {
+  const int n = block_plan(p, block_of(p, u)).count();
+  return n > 0 ? n + kSwitchCost : 0;
+}
+
+// Exclusive prefix sum of cost(k) over k in [0, n) into out[0..n] (out[n] =
+// total), by one CTA of kPrepThreads threads; returns the total.
+template <typename Cost>
+__device__ int prefix_costs(int n, Cost cost, int32_t* out) {
   __shared__ int32_t warp_sums[kPrepThreads / 32];
   __shared__ int32_t carry;
   constexpr int kWarps = kPrepThreads / 32;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  for (int base = 0; base < p.blocks; base += kPrepThreads) {
+  for (int base = 0; base < n; base += kPrepThreads) {
     const int u = base + threadIdx.x;
-    int n = 0;
-    if (u < p.blocks) {
-      n = block_plan(p, block_of(p, u)).count();
-      if (n > 0) n += kSwitchCost;
-    }
-    int incl = n;  // inclusive scan within the warp
+    const int c = u < n ? cost(u) : 0;
+    int incl = c;  // inclusive scan within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -225,12 +245,94 @@ __device__ void plan_units(const AttnParams& p) {
     }
     __syncthreads();
     const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    if (u < p.blocks) p.ustart[u] = before + incl - n;
+    if (u < n) out[u] = before + incl - c;
     __syncthreads();
     if (threadIdx.x == kPrepThreads - 1) carry = before + incl;
     __syncthreads();
   }
-  if (threadIdx.x == 0) p.ustart[p.blocks] = carry;
+  if (threadIdx.x == 0) out[n] = carry;
+  return carry;
+}
+
+// First position of team t's blocks when `nb` blocks, sorted by cost, are
+// dealt to `teams` teams in rounds of alternating direction (round r gives
+// sorted position r*teams + j to team j, or to team teams-1-j when r is odd).
+__device__ __forceinline__ int deal_start(int t, int nb, int teams) {
+  const int R = nb / teams, rem = nb % teams;
+  return t * R + ((R & 1) == 0 ? min(t, rem) : max(0, t - (teams - rem)));
+}
+
+// Cost of every block (its live key tiles plus the switch cost) and the
+// exclusive prefix sum of the costs, by one CTA of kPrepThreads threads.
+// With p.perm, blocks are first dealt whole to the teams, largest first in
+// rounds of alternating direction; that deal is kept when its busiest team
+// carries at most the even split's share plus kCutCost, and then no unit is
+// cut (no partial rows, nothing to merge).  Otherwise, and always without
+// p.perm, the teams split the costs in index order evenly.  With p.perm the
+// walk order goes to p.uorder (and its inverse to p.upos) and the team ranges
+// to p.tlo.
+__device__ void plan_units(const AttnParams& p) {
+  if (!p.perm) {
+    prefix_costs(p.blocks, [&](int u) { return block_cost(p, u); }, p.ustart);
+    return;
+  }
+  __shared__ int32_t cost[kPlanSortMax];
+  __shared__ int32_t order[kPlanSortMax];
+  __shared__ int32_t total, biggest, busiest;
+  const int NB = p.blocks, teams = p.teams;  // NB <= kPlanSortMax (host)
+  if (threadIdx.x == 0) {
+    total = 0;
+    biggest = 0;
+    busiest = 0;
+  }
+  __syncthreads();
+  int sum = 0, mx = 0;
+  for (int u = threadIdx.x; u < NB; u += kPrepThreads) {
+    const int c = block_cost(p, u);
+    cost[u] = c;
+    sum += c;
+    mx = max(mx, c);
+  }
+  atomicAdd(&total, sum);
+  atomicMax(&biggest, mx);
+  __syncthreads();
+  const int T = total;
+  const int even = (T + teams - 1) / teams + kCutCost;
+  bool whole = biggest <= even;
+  if (whole) {
+    for (int u = threadIdx.x; u < NB; u += kPrepThreads) {
+      const int c = cost[u];
+      int rank = 0;  // position in decreasing cost, ties by block index
+      for (int v = 0; v < NB; ++v) rank += (cost[v] > c) || (cost[v] == c && v < u);
+      const int r = rank / teams, j = rank % teams;
+      order[deal_start((r & 1) ? teams - 1 - j : j, NB, teams) + r] = u;
+    }
+    __syncthreads();
+    int worst = 0;
+    for (int t = threadIdx.x; t < teams; t += kPrepThreads) {
+      int load = 0;
+      for (int k = deal_start(t, NB, teams), e = deal_start(t + 1, NB, teams); k < e; ++k) load += cost[order[k]];
+      worst = max(worst, load);
+    }
+    atomicMax(&busiest, worst);
+    __syncthreads();
+    whole = busiest <= even;  // the same value in every thread
+  }
+  if (!whole) {
+    for (int k = threadIdx.x; k < NB; k += kPrepThreads) order[k] = k;
+    __syncthreads();
+  }
+  for (int k = threadIdx.x; k < NB; k += kPrepThreads) {
+    p.uorder[k] = order[k];
+    p.upos[order[k]] = k;
+  }
+  prefix_costs(NB, [&](int k) { return cost[order[k]]; }, p.ustart);
+  __syncthreads();  // ustart, written by other threads of this CTA
+  for (int t = threadIdx.x; t <= teams; t += kPrepThreads)
+    p.tlo[t] = t == teams ? T
+                          : (whole ? p.ustart[deal_start(t, NB, teams)]
+                                   : static_cast<int32_t>(static_cast<long long>(T) * t / teams));
+  if (threadIdx.x == 0) p.tlo[teams + 1] = whole ? 1 : 0;  // whole blocks: no unit is cut
 }
 
 // CTA 0 plans (plan_units); the others rotate the chunk's queries and
@@ -363,7 +465,7 @@ __device__ __forceinline__ void deal_mask32(float (&mv)[32], const float4 (&v)[8
 // SINK: the implicit mask also keeps pinned sink slots visible (a separate
 // instantiation, so the common case carries none of that code).  F16: an
 // fp16 KV cache, every product in fp16.
-template <int D, bool EXPLICIT, bool SINK, bool F16>
+template <int D, bool EXPLICIT, bool SINK, bool F16, bool PERM>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                      const __grid_constant__ CUtensorMap map_kn, const __grid_constant__ CUtensorMap map_vn,
@@ -418,7 +520,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t tmem = bars->tmem_base;
   uint8_t* sK = smem + CF::kK;
   uint8_t* sV = smem + CF::kV;
-  SegWalk walk;
+  SegWalk<PERM> walk;
   walk.init(p, cta);
 
   if (warp >= 8) {
@@ -899,7 +1001,7 @@ constexpr int kMergePieceBatch = 2;
 // a unit has two pieces, the usual case).  Registers are capped at 64 so that
 // four blocks fit an SM: the grid then runs in under two waves (at 90
 // registers it took 3.4).
-template <int D>
+template <int D, bool PERM>
 __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const AttnParams p) {
   __shared__ int piece_slot[kMaxCtas];  // partial-result slot of each piece, in CTA order
   __shared__ int n_pieces;
@@ -912,16 +1014,21 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
   if (p.app_n && blockIdx.x == 0 && blockIdx.y == 0)  // fused append: every reader of len is done
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) fused_append_len(p, b);
   if (warp == 0) {
-    const int gblk = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
+    const int gnat = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
+    const int gblk = PERM ? p.upos[gnat] : gnat;  // the block's place in the walk order
     const int member = x.pair % p.team;
     const long long s0 = p.ustart[gblk], s1 = p.ustart[gblk + 1];
     const long long T = p.ustart[p.blocks];
     int np = 0;
-    if (s1 > s0) {
-      // team t covers cost positions [floor(t T / teams), floor((t+1) T / teams));
-      // the last team whose range starts at or before x is floor(((x + 1) teams - 1) / T).
-      const int t_first = static_cast<int>(((s0 + 1) * p.teams - 1) / T);
-      const int t_last = static_cast<int>((s1 * p.teams - 1) / T);
+    if (PERM && s1 > s0 && p.tlo[p.teams + 1]) {
+      np = -1;  // whole blocks were dealt: one CTA wrote every row of the unit
+    } else if (s1 > s0) {
+      // teams whose ranges meet [s0, s1): from the last team whose range starts
+      // at or before s0 to the last one starting at or before s1 - 1; even
+      // split: team t covers [floor(t T / teams), floor((t+1) T / teams)), and the
+      // last team starting at or before x is floor(((x + 1) teams - 1) / T)
+      const int t_first = PERM ? unit_at(p.tlo, p.teams, s0) : static_cast<int>(((s0 + 1) * p.teams - 1) / T);
+      const int t_last = PERM ? unit_at(p.tlo, p.teams, s1 - 1) : static_cast<int>((s1 * p.teams - 1) / T);
       for (int t0 = t_first; t0 <= t_last; t0 += 32) {
         const int t = t0 + lane;
         int slot = -1;
@@ -1036,6 +1143,10 @@ PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms) {
                              ((P + kBN - 1) / kBN + (C + kBN - 1) / kBN + kSwitchCost);
   t.teams = static_cast<int>(max(1LL, min(static_cast<long long>(sms / t.team), max_cost)));
   t.ctas = t.teams * t.team;
+  // small teams (chunks of at most 512 packed rows per (sequence, kv head))
+  // and at least one block per team: the plan may deal whole blocks instead
+  // of cutting them (with fewer blocks than teams the even split is kept)
+  t.perm = t.team <= 2 && t.teams > 1 && t.blocks >= t.teams && t.blocks <= kPlanSortMax ? 1 : 0;
   return t;
 }
 
@@ -1045,6 +1156,9 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
   PairWorkspace w;
   size_t off = 0;
   w.ustart = off; off += al((static_cast<size_t>(t.blocks) + 1) * sizeof(int32_t));
+  w.uorder = off; off += al(static_cast<size_t>(t.blocks) * sizeof(int32_t));
+  w.upos = off; off += al(static_cast<size_t>(t.blocks) * sizeof(int32_t));
+  w.tlo = off; off += al((static_cast<size_t>(t.teams) + 2) * sizeof(int32_t));  // + the whole-deal flag
   w.part_o = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * D * sizeof(float));
   w.part_lse = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * sizeof(float));
   w.ptag = off; off += al(static_cast<size_t>(ctas) * 2 * sizeof(int32_t));
@@ -1055,10 +1169,10 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
   return w;
 }
 
-template <int D, bool EXPLICIT, bool SINK, bool F16>
+template <int D, bool EXPLICIT, bool SINK, bool F16, bool PERM>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   constexpr int smem = pair_smem_bytes<D, EXPLICIT>();
-  auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16>;
+  auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16, PERM>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1074,15 +1188,16 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
   e = launch_dependent(kern, dim3(p.ctas), dim3(kThreadsPair), smem, stream, maps[0], maps[1], maps[2], maps[3],
                        maps[4], p);
   if (e != cudaSuccess) return e;
-  return launch_dependent(merge_units_kernel<D>, dim3(p.units, kUnitRows / kMergeRows), dim3(kMergeThreads), 0,
+  return launch_dependent(merge_units_kernel<D, PERM>, dim3(p.units, kUnitRows / kMergeRows), dim3(kMergeThreads), 0,
                           stream, p);
 }
 
 template <int D, bool F16>
 static cudaError_t launch_pair_d(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  if (p.mask) return launch_pair_t<D, true, false, F16>(maps, p, stream);
-  if (p.sink > 0) return launch_pair_t<D, false, true, F16>(maps, p, stream);
-  return launch_pair_t<D, false, false, F16>(maps, p, stream);
+  if (p.mask) return launch_pair_t<D, true, false, F16, false>(maps, p, stream);
+  if (p.sink > 0) return launch_pair_t<D, false, true, F16, false>(maps, p, stream);
+  if (p.perm) return launch_pair_t<D, false, false, F16, true>(maps, p, stream);
+  return launch_pair_t<D, false, false, F16, false>(maps, p, stream);
 }
 
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {

@@ -44,7 +44,12 @@ struct AttnParams {
   float* part_lse;  // [splits][B][Hq][C]
   int32_t* err;
   // persistent team-aligned stream-K path (two query tiles per work unit)
-  int32_t* ustart;  // [blocks + 1] exclusive prefix sum of block costs
+  int32_t* ustart;  // [blocks + 1] exclusive prefix sum of block costs, in walk order
+  int perm;         // blocks walked in the planned order uorder, team ranges in tlo
+  int32_t* uorder;  // [blocks] block at each walk position (perm)
+  int32_t* upos;    // [blocks] walk position of each block (perm)
+  int32_t* tlo;     // [teams + 2] first cost position of each team's range, the total,
+                    // then 1 when whole blocks were dealt (perm)
   int units;        // B * Hkv * pairs
   int pairs;        // query-tile pairs per (sequence, kv head)
   int team;         // CTAs per team = pairs per block
@@ -77,10 +82,11 @@ struct AttnParams {
 // Team-aligned stream-K layout for these sizes, and its workspace.
 struct PairTeams {
   int pairs, team, nblk, blocks, teams, ctas;
+  int perm;  // the plan may reorder blocks (whole-block deal); implicit masks without sinks only
 };
 PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms);
 struct PairWorkspace {
-  size_t ustart, part_o, part_lse, ptag, q_rot, k_rot, v_cvt, total;
+  size_t ustart, uorder, upos, tlo, part_o, part_lse, ptag, q_rot, k_rot, v_cvt, total;
 };
 PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t);
 // maps for the pair path: cache K, cache V, rotated chunk K, chunk V, rotated Q

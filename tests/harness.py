@@ -50,15 +50,21 @@ def two_tile_path(D, Hq, Hkv, C):
 
 def assert_explicit_matches(out_e, out_i, two_tile, what=""):
     """Outputs of the explicit and the implicit form of one mask: bitwise
-    identical, except on the two-tile kernel, whose explicit path rounds the
-    masked, scaled score once before the row max is subtracted where the
-    implicit path fuses both steps: there within rounding."""
+    identical, except on the two-tile kernel.  There the explicit path rounds
+    the masked, scaled score once before the row max is subtracted where the
+    implicit path fuses both steps, and the two forms may split the work
+    differently: the implicit form's plan can deal whole (sequence, kv head)
+    blocks to the CTAs while the explicit form, which visits every key tile,
+    is split evenly with units cut between CTAs and merged.  P is then rounded
+    to bf16 against different running maxima, so the two agree within the
+    output tolerance (max-abs 1e-2, rel-L2 3e-3), as each does with the
+    oracle."""
     if not two_tile:
         assert torch.equal(out_e.view(torch.int16), out_i.view(torch.int16)), f"{what}: explicit != implicit"
         return
     ref = out_i.detach().float().cpu().numpy().astype(np.float64)
     max_abs, rel = compare(out_e, ref, what)
-    assert max_abs <= MAX_ABS and rel <= 1e-3, f"{what}: explicit vs implicit max_abs={max_abs:.3e} rel_l2={rel:.3e}"
+    assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: explicit vs implicit max_abs={max_abs:.3e} rel_l2={rel:.3e}"
 
 
 def check_argmax(gpu_sel: torch.Tensor, ref_sel: np.ndarray, what=""):

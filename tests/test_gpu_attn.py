@@ -1,8 +1,9 @@
 """GPU parity of chunk-prefill attention and decode against the fp64 oracle.
 
 Outputs within max-abs 1e-2 and rel-L2 3e-3 of the oracle; explicit and
-implicit masks bitwise identical (within rounding on the two-tile kernel, whose
-explicit path rounds the masked score before subtracting the max); two runs
+implicit masks bitwise identical (within that tolerance on the two-tile kernel,
+whose explicit path rounds the masked score before subtracting the max and
+whose two forms may split the work differently); two runs
 bitwise identical; selected-row
 argmax exact unless the oracle's top-2 gap is within tolerance.
 Sources: "functiongemma: chunk prefill-with-past graph gemma_prefill_with_past"
@@ -261,6 +262,64 @@ def test_packed_batch_full_size_explicit_mask_sampled():
     order = np.argsort(L.numpy())
     pairs = [(int(order[0]), 1), (int(order[-1]), 6), (int(order[len(order) // 2]), 4)]
     sample_check(cpa, w, pairs, device_gen=True, explicit=True)
+
+
+def test_packed_batch_every_unit_implicit_matches_explicit():
+    """The full packed batch: with the implicit mask the plan deals whole
+    (sequence, kv head) blocks to the teams (no unit cut), with the explicit
+    mask it splits the key tiles evenly and merges cut units.  Every output row
+    of the two agrees within rounding, so no unit of the whole-block deal is
+    skipped or misplaced."""
+    cpa = lib()
+    w = WORKLOADS["packed_batch"]
+    out_e = sample_check(cpa, w, [], device_gen=True, explicit=True)
+    out_i = sample_check(cpa, w, [], device_gen=True)
+    assert_explicit_matches(out_e, out_i, True, "packed_batch/all units")
+
+
+def test_whole_block_deal_every_unit():
+    """64 sequences, 16/4 heads, D 64, C 64, past lengths uniform on [128, 384]:
+    256 (sequence, kv head) blocks of 5 to 7 key tiles (switch cost included)
+    for about 150 one-CTA teams.  The largest block fits the even split's share
+    plus the cut cost, and the deal (largest first, rounds of alternating
+    direction) gives no team more than that, so every unit is finished whole by
+    one CTA.  Every row against the oracle; the explicit form of the same mask
+    (even split, cut units merged) agrees within rounding."""
+    cpa = lib()
+    w = small("whole_deal", 64, 16, 4, 64, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64))
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    out, sel, err = run_gpu(cpa, inp, ck, cv, w.P)
+    assert int(err[0]) == 0
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                               inp["past_len"], inp["n_real"], sel_row=inp["n_real"] - 1)
+    assert_close(out, ref, w.name)
+    check_argmax(sel, ref_sel, w.name)
+    mask = explicit_masks(inp["past_len"], inp["n_real"], w.C, w.P, w.Hq, 0, 1)
+    out_e, _, err = run_gpu(cpa, inp, ck, cv, w.P, mask=mask)
+    assert int(err[0]) == 0
+    assert_explicit_matches(out_e, out, True, w.name)
+
+
+def test_planned_walk_even_split_fallback():
+    """80 (sequence, kv head) blocks for 74-76 two-CTA teams (20 sequences,
+    32/4 heads, D 128, C 64), 19 sequences with pasts of 200 to 380 rows and
+    one with 4000: the largest block (36 tiles with the switch cost) exceeds
+    the even split's share plus the cut cost, so the plan keeps the even split
+    inside the planned-order walk and cuts that block between teams.  Every
+    row (each sees at least 200 keys) against the oracle."""
+    cpa = lib()
+    w = small("plan_fallback", 20, 32, 4, 128, 64, 4096, ("uniform", 200, 380), ("uniform", 1, 64))
+    L = w.past_lens().clone()
+    L[7] = 4000
+    inp = make_chunk_inputs(w, past_len=L)
+    ck, cv = make_cache(w)
+    out, sel, err = run_gpu(cpa, inp, ck, cv, w.P)
+    assert int(err[0]) == 0
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P,
+                               inp["past_len"], inp["n_real"], sel_row=inp["n_real"] - 1)
+    assert_close(out, ref, w.name)
+    check_argmax(sel, ref_sel, w.name)
 
 
 def test_long_context_full_size_sampled():

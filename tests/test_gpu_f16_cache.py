@@ -8,7 +8,7 @@ through a padded tail with snapshot and rollback); the attention runs its
 products in fp16 on every path (two-tile, single-tile with and without a
 cluster, decode, explicit mask, fused append) and matches the oracle within
 the attention tolerance; explicit and implicit masks give the same bits
-(within rounding on the two-tile kernel).
+(within the output tolerance on the two-tile kernel).
 """
 import numpy as np
 import pytest

@@ -10,7 +10,7 @@ runs the implicit mask and the explicit mask built from the same rule
 ("functiongemma: chunk prefill-with-past graph", Change: per-head additive mask
 over past + C keys) and checks both against the oracle (max-abs 1e-2, rel-L2
 3e-3), the selected-row argmax, and the two masks against each other (bitwise,
-or within rounding on the two-tile kernel).
+or within the output tolerance on the two-tile kernel).
 """
 import numpy as np
 import pytest
