@@ -140,8 +140,10 @@ typedef struct {
  *   out_sel  fp32 [B, Hq*D] or NULL: row sel_row[b] of every head, before
  *          bf16 rounding.
  *   workspace  device memory of at least cpa_attn_workspace_size(...) bytes
- *          (split-KV partial results, rotated copies of the chunk's queries
- *          and keys); may be NULL when that size is 0.
+ *          (the work plan the call builds on the device, split-KV partial
+ *          results, rotated copies of the chunk's queries and keys); may be
+ *          NULL when that size is 0.  Its contents need no initialisation
+ *          and are meaningless after the call.
  *   err    device int32 error word (required).
  *   sm_budget  0, or the number of SMs the call may occupy: a value below
  *          the device's SM count sizes the persistent grid for that many
