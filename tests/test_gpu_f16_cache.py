@@ -36,6 +36,10 @@ CASES = [
     small("h_single_g32_c1", 2, 32, 1, 128, 1, 600, ("uniform", 100, 600), ("fixed", 1), causal=0),
     small("h_decode", 3, 8, 2, 128, 1, 700, ("uniform", 1, 700), ("fixed", 1), causal=0),
     small("h_decode_d64_win", 2, 8, 2, 64, 1, 900, ("uniform", 300, 900), ("fixed", 1), window=100, causal=0),
+    # more (sequence, kv head) blocks than one-CTA teams, all of similar cost:
+    # the plan deals whole blocks to the teams (the planned-order walk)
+    small("h_whole_deal_d64", 64, 16, 4, 64, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64)),
+    small("h_whole_deal_d128", 48, 16, 4, 128, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64)),
 ]
 
 
@@ -129,7 +133,7 @@ def test_f16_sliding_padded_tail_equals_exact_append(prefix, tail):
     assert np.array_equal(bits16(cache.v)[:, :, :Lf], ov_[:, :, :Lf])
 
 
-@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[5]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[5], CASES[-1]], ids=lambda w: w.name)
 def test_f16_fused_append_equals_attention_then_append(w):
     cpa = lib()
     inp = {k: v.to(DEV) for k, v in make_chunk_inputs(w).items()}

@@ -32,6 +32,8 @@ CASES = [
     case("fa_single_d64_small", 2, 4, 1, 64, 16, 48, ("uniform", 0, 48), ("uniform", 1, 16)),
     case("fa_single_g32_c1", 2, 32, 1, 128, 1, 4096, ("uniform", 1000, 4096), ("fixed", 1)),
     case("fa_decode", 4, 8, 2, 128, 1, 1024, ("uniform", 1, 1024), ("fixed", 1)),
+    # more blocks than one-CTA teams, of similar cost: whole blocks dealt to the teams
+    case("fa_whole_deal", 48, 16, 4, 128, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64)),
 ]
 
 
