@@ -2,6 +2,8 @@
 // split-KV policy and kernel launches.  Nothing here allocates device memory
 // or synchronises.
 #include <math.h>
+
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -47,10 +49,15 @@ bool make_map(CUtensorMap* m, const void* base, int D, int rows, int heads, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device, queried once per device (devices 0-63).
 int num_sms() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
+  static std::atomic<int> cached[64];
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 enum Path { kPathSingle = 0, kPathPair = 1, kPathDecode = 2 };
@@ -311,6 +318,18 @@ cpa_status chunk_check(const void* k_new, const void* v_new, const float* cos, c
 }
 
 }  // namespace
+
+namespace cpa {
+
+size_t attn_workspace_need(const cpa_attn_args* a) {
+  if (!a || a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->C < 1 || a->P < 0 || a->Hq % a->Hkv ||
+      a->Hq / a->Hkv > 128 || !valid_d(a->D) || a->sm_budget < 0)
+    return 0;
+  const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, a->sm_budget);
+  return workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C);
+}
+
+}  // namespace cpa
 
 extern "C" {
 

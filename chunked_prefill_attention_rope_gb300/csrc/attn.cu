@@ -765,12 +765,8 @@ template <int D, int BN, bool F16>
 static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   using SM = AttnSmem<D, BN>;
   auto kern = attn_kernel<D, BN, F16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static SmemAttr smem_attr;
+  if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), SM::kAlloc); e != cudaSuccess) return e;
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
   const long long items = static_cast<long long>(p.B) * p.Hkv * p.C * (D / 16);
   const int kblocks = static_cast<int>(max(1LL, min(static_cast<long long>(152) * 8, (items + 255) / 256)));

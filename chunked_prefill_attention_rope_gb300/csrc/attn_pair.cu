@@ -1173,12 +1173,8 @@ template <int D, bool EXPLICIT, bool SINK, bool F16, bool PERM>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   constexpr int smem = pair_smem_bytes<D, EXPLICIT>();
   auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16, PERM>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static SmemAttr smem_attr;
+  if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), smem); e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.B) * ((p.Hq + p.Hkv + kPrepHeads - 1) / kPrepHeads) * p.C *
                           (p.D / 16);
   const int rope_blocks =

@@ -427,12 +427,8 @@ template <int D, bool EXPLICIT, bool F16>
 static cudaError_t launch_decode_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   using CF = DecCfg<D>;
   auto kern = attn_decode_kernel<D, EXPLICIT, F16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static SmemAttr smem_attr;
+  if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), CF::kSmem); e != cudaSuccess) return e;
   dim3 grid(p.splits, p.Hkv, p.B);
   return launch_dependent(kern, grid, dim3(kDThreads), CF::kSmem, stream, maps[0], maps[1], maps[2], maps[3], p);
 }

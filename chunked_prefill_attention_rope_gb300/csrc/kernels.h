@@ -5,7 +5,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
+#include "../../include/cpa.h"
+
 namespace cpa {
+
+// Raises a kernel's dynamic shared-memory limit once per device.  The
+// attribute belongs to the current device's context, so each device keeps
+// its own bit (devices 0-63; beyond that the attribute is set on every
+// launch).  Two host threads racing on one device both set it, which is
+// harmless.
+struct SmemAttr {
+  std::atomic<uint64_t> done{0};
+  cudaError_t ensure(const void* kern, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
+// Workspace bytes the attention call described by `a` needs, sized for its
+// own sm_budget (0 for sizes the call would reject).
+size_t attn_workspace_need(const cpa_attn_args* a);
 
 // Launch `kern` as a programmatic dependent of the grid before it on the
 // stream: it may start while that grid runs and must call

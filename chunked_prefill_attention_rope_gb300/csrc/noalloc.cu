@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
@@ -43,7 +44,8 @@ void* scratch_address() {
 
 extern "C" cpa_status cpa_chunk_prefill_attn_noalloc(const cpa_attn_args* args, cpa_stream stream) {
   if (!args) return CPA_ERR_NULL;
-  const size_t need = cpa_attn_workspace_size(args->B, args->Hq, args->Hkv, args->D, args->C, args->P);
+  // sized for the call's own SM budget (a partial budget needs fewer partial slots)
+  const size_t need = cpa::attn_workspace_need(args);
   if (need > kStaticScratchBytes) return CPA_ERR_WORKSPACE;
   cpa_attn_args a = *args;
   a.workspace = nullptr;

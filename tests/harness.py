@@ -115,3 +115,38 @@ def explicit_masks(past_len, n_real, C, P, Hq, window, causal, sink=0):
     for b in range(B):
         out[b] = O.explicit_mask(int(past_len[b]), int(n_real[b]), C, P, window, causal, sink)[None]
     return torch.from_numpy(out)
+
+
+def sample_rows(C, R, n, salt=0):
+    """Chunk rows to check in one (sequence, kv head) group: the first, one
+    inner and the last row of every R-row query tile, plus the last real row."""
+    rows = set()
+    for t0 in range(0, C, R):
+        hi = min(t0 + R, C)
+        rows.update((t0, t0 + (7 * (t0 // R) + 5 + salt) % (hi - t0), hi - 1))
+    if n > 0:
+        rows.add(n - 1)
+    return sorted(rows)
+
+
+def oracle_rows(q, k_new, v_new, cos, sin, ck, cv, L, n, rows, window=0, causal=1):
+    """fp64 outputs of chunk rows `rows` of one (sequence, kv head) group,
+    composed from the oracle's own steps: RoPE of the sampled query rows and of
+    every chunk key, the implicit mask's rows, and softmax attention.  Inputs
+    are host tensors of one group: q [G, C, D], k_new/v_new [C, D], cos/sin
+    [C, D], cache rows ck/cv [L, D] (the L valid past slots; slots past L are
+    masked and never read).  Returns [G, len(rows), D]."""
+    G, C, D = q.shape
+    rows = np.asarray(rows)
+    c = cos.numpy()
+    s = sin.numpy()
+    k_rot = O.bf16_to_f32(O.rope_rotate(bf16_bits(k_new), c, s)).astype(np.float64)
+    keys = np.concatenate([O.bf16_to_f32(bf16_bits(ck)).astype(np.float64), k_rot], axis=0)
+    vals = np.concatenate([O.bf16_to_f32(bf16_bits(cv)).astype(np.float64),
+                           O.bf16_to_f32(bf16_bits(v_new)).astype(np.float64)], axis=0)
+    m = O.explicit_mask(L, n, C, L, window, causal)[rows]
+    out = np.zeros((G, len(rows), D))
+    for g in range(G):
+        qr = O.bf16_to_f32(O.rope_rotate(bf16_bits(q[g, rows]), c[rows], s[rows])).astype(np.float64)
+        out[g] = O.attend(qr, keys, vals, m, 1.0 / np.sqrt(D))
+    return out

@@ -18,7 +18,7 @@ import torch
 import oracle as O
 from synth import WORKLOADS, Workload, make_chunk_inputs, make_cache, normal_bf16, rope_tables
 from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks, two_tile_path,
-                     assert_explicit_matches)
+                     assert_explicit_matches, sample_rows, oracle_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -208,11 +208,10 @@ def test_page1_shape_eighteen_layers_explicit_masks():
         assert torch.equal(out_i.view(torch.int16), out.view(torch.int16)), f"page1/L{layer} implicit"
 
 
-def sample_check(cpa, w, pairs, device_gen=False, explicit=False):
-    """Run the full workload on the GPU, check sampled (b, kv-head) groups on the
-    oracle.  `explicit`: pass the mask as an explicit [B, Hq, C, P+C] tensor,
-    each sequence's rows built by the oracle's mask function and repeated over
-    the heads on the device."""
+def run_full(cpa, w, device_gen=False, explicit=False):
+    """Run the full workload on the GPU.  `explicit`: pass the mask as an
+    explicit [B, Hq, C, P+C] tensor, each sequence's rows built by the
+    oracle's mask function and repeated over the heads on the device."""
     dev = DEV if device_gen else "cpu"
     inp = make_chunk_inputs(w, device=dev)
     ck, cv = make_cache(w, device=dev)
@@ -230,50 +229,48 @@ def sample_check(cpa, w, pairs, device_gen=False, explicit=False):
     del mask
     torch.cuda.synchronize()
     assert int(err[0]) == 0
+    return out, inp, ck, cv
+
+
+def check_every_group(w, out, inp, ck, cv, salt=0):
+    """Every (sequence, kv head) group against the oracle on sampled rows:
+    the first, an inner and the last row of every query tile and the last
+    real row, for every q head of the group."""
     G = w.Hq // w.Hkv
-    u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    for b, kvh in pairs:
-        hs = slice(kvh * G, (kvh + 1) * G)
-        L = int(inp["past_len"][b])
-        ref, _ = O.chunk_prefill_attn(
-            u16(inp["q"][b:b + 1, hs]), u16(inp["k"][b:b + 1, kvh:kvh + 1]),
-            u16(inp["v"][b:b + 1, kvh:kvh + 1]), inp["cos"][b:b + 1].cpu().numpy(),
-            inp["sin"][b:b + 1].cpu().numpy(), u16(ck[b:b + 1, kvh:kvh + 1, :L]),
-            u16(cv[b:b + 1, kvh:kvh + 1, :L]), L, [L], [int(inp["n_real"][b])], causal=w.causal)
-        assert_close(out[b:b + 1, hs], ref, f"{w.name}/b{b}/kvh{kvh}")
-    return out
+    R = max(1, 128 // G)
+    host = lambda t: t.detach().cpu()
+    out_h = host(out)
+    for b in range(w.B):
+        L, n = int(inp["past_len"][b]), int(inp["n_real"][b])
+        rows = sample_rows(w.C, R, n, salt + b)
+        q_b, k_b, v_b = host(inp["q"][b]), host(inp["k"][b]), host(inp["v"][b])
+        cos_b, sin_b = host(inp["cos"][b]), host(inp["sin"][b])
+        for kvh in range(w.Hkv):
+            hs = slice(kvh * G, (kvh + 1) * G)
+            ref = oracle_rows(q_b[hs], k_b[kvh], v_b[kvh], cos_b, sin_b, host(ck[b, kvh, :L]),
+                              host(cv[b, kvh, :L]), L, n, rows, w.window, w.causal)
+            assert_close(out_h[b, hs][:, rows], ref, f"{w.name}/b{b}/kvh{kvh}")
 
 
-def test_packed_batch_full_size_sampled():
+def test_packed_batch_full_size_every_group():
+    """Every (sequence, kv head) group of the packed batch (B 16, 32/8 heads,
+    D 128, past U[0, 4095], C 128), 13 rows of each of its 32 q heads."""
     cpa = lib()
     w = WORKLOADS["packed_batch"]
-    L = w.past_lens()
-    order = np.argsort(L.numpy())
-    pairs = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
-    sample_check(cpa, w, pairs)
+    out, inp, ck, cv = run_full(cpa, w)
+    check_every_group(w, out, inp, ck, cv)
 
 
-def test_packed_batch_full_size_explicit_mask_sampled():
+def test_packed_batch_full_size_explicit_mask_every_group():
     """The packed batch with its 1.1 GB explicit fp32 mask, in the launch
-    configuration the bench times."""
+    configuration the bench times: every group against the oracle, and the
+    whole output bitwise equal to the implicit form's."""
     cpa = lib()
     w = WORKLOADS["packed_batch"]
-    L = w.past_lens()
-    order = np.argsort(L.numpy())
-    pairs = [(int(order[0]), 1), (int(order[-1]), 6), (int(order[len(order) // 2]), 4)]
-    sample_check(cpa, w, pairs, device_gen=True, explicit=True)
-
-
-def test_packed_batch_every_unit_implicit_matches_explicit():
-    """The full packed batch: with the implicit mask the plan deals whole
-    (sequence, kv head) blocks to the teams (no unit cut), with the explicit
-    mask it splits the key tiles evenly and merges cut units.  Every output row
-    of the two agrees within rounding, so no unit of the whole-block deal is
-    skipped or misplaced."""
-    cpa = lib()
-    w = WORKLOADS["packed_batch"]
-    out_e = sample_check(cpa, w, [], device_gen=True, explicit=True)
-    out_i = sample_check(cpa, w, [], device_gen=True)
+    out_e, inp, ck, cv = run_full(cpa, w, device_gen=True, explicit=True)
+    check_every_group(w, out_e, inp, ck, cv, salt=3)
+    del ck, cv
+    out_i, _, _, _ = run_full(cpa, w, device_gen=True)
     assert_explicit_matches(out_e, out_i, True, "packed_batch/all units")
 
 
@@ -284,7 +281,7 @@ def test_whole_block_deal_every_unit():
     plus the cut cost, and the deal (largest first, rounds of alternating
     direction) gives no team more than that, so every unit is finished whole by
     one CTA.  Every row against the oracle; the explicit form of the same mask
-    (even split, cut units merged) agrees within rounding."""
+    gives the same bits."""
     cpa = lib()
     w = small("whole_deal", 64, 16, 4, 64, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64))
     inp = make_chunk_inputs(w)
@@ -307,7 +304,8 @@ def test_planned_walk_even_split_fallback():
     one with 4000: the largest block (36 tiles with the switch cost) exceeds
     the even split's share plus the cut cost, so the plan keeps the even split
     inside the planned-order walk and cuts that block between teams.  Every
-    row (each sees at least 200 keys) against the oracle."""
+    row (each sees at least 200 keys) against the oracle; the explicit form of
+    the same mask takes the same plan and gives the same bits."""
     cpa = lib()
     w = small("plan_fallback", 20, 32, 4, 128, 64, 4096, ("uniform", 200, 380), ("uniform", 1, 64))
     L = w.past_lens().clone()
@@ -320,14 +318,25 @@ def test_planned_walk_even_split_fallback():
                                inp["past_len"], inp["n_real"], sel_row=inp["n_real"] - 1)
     assert_close(out, ref, w.name)
     check_argmax(sel, ref_sel, w.name)
+    mask = explicit_masks(inp["past_len"], inp["n_real"], w.C, w.P, w.Hq, 0, 1)
+    out_e, _, err = run_gpu(cpa, inp, ck, cv, w.P, mask=mask)
+    assert int(err[0]) == 0
+    assert_explicit_matches(out_e, out, True, w.name)
 
 
-def test_long_context_full_size_sampled():
+def test_long_context_full_size_every_group():
+    """All 32 (sequence, kv head) groups of the long-context chunk (B 4, 32/8
+    heads, D 128, past 32768, C 512): the plan cuts these units between the
+    CTAs of a team and merges their pieces, so every group and every query
+    tile is checked."""
     cpa = lib()
-    sample_check(cpa, WORKLOADS["long_ctx"], [(0, 0), (3, 7)], device_gen=True)
+    w = WORKLOADS["long_ctx"]
+    out, inp, ck, cv = run_full(cpa, w, device_gen=True)
+    check_every_group(w, out, inp, ck, cv)
 
 
-def test_decode_full_size_sampled():
+def test_decode_full_size_every_group():
+    """Every q head of all 64 decode sequences (past U[1024, 32768])."""
     cpa = lib()
     w = WORKLOADS["decode"]
     inp = make_chunk_inputs(w, device=DEV)
@@ -340,17 +349,17 @@ def test_decode_full_size_sampled():
     assert int(err[0]) == 0
     G = w.Hq // w.Hkv
     Ls = inp["past_len"].cpu().numpy()
-    picks = [int(np.argmin(Ls)), int(np.argmax(Ls)), 17]
     u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    for b in picks:
-        for kvh in (0, 5):
-            L = int(Ls[b])
+    out_h = out.cpu()
+    for b in range(w.B):
+        L = int(Ls[b])
+        for kvh in range(w.Hkv):
             hs = slice(kvh * G, (kvh + 1) * G)
             ref = O.decode_step(u16(inp["q"][b:b + 1, hs]), u16(inp["k"][b:b + 1, kvh:kvh + 1]),
                                 u16(inp["v"][b:b + 1, kvh:kvh + 1]), inp["cos"][b:b + 1].cpu().numpy(),
                                 inp["sin"][b:b + 1].cpu().numpy(), u16(ck[b:b + 1, kvh:kvh + 1, :L]),
                                 u16(cv[b:b + 1, kvh:kvh + 1, :L]), L, [L])
-            assert_close(out[b:b + 1, hs], ref, f"decode/b{b}/kvh{kvh}")
+            assert_close(out_h[b:b + 1, hs], ref, f"decode/b{b}/kvh{kvh}")
 
 
 def test_out_of_range_lengths_are_flagged_and_clamped():

@@ -9,13 +9,18 @@ bytes, the same lengths and error bits.  Every attention path is covered (the
 two-tile kernel, the single-tile kernel with a cluster merge and with the
 combine kernel, the one-token decode kernel), with past_len passed as its own
 tensor and as the cache's own len, an explicit mask, n_rows different from
-n_real, and a sequence whose append overflows the cache.
+n_real, and a sequence whose append overflows the cache.  The fused call is
+also compared with the fp64 oracle directly (attention then global append):
+outputs within the attention tolerance, the selected-row argmax by the tie
+rule, cache rows [0, len) and len bit-exact.
 """
+import numpy as np
 import pytest
 import torch
 
-from synth import Workload, make_chunk_inputs, make_cache
-from harness import lib, explicit_masks
+import oracle as O
+from synth import Workload, make_chunk_inputs, make_cache, bf16_bits
+from harness import lib, explicit_masks, oracle_attn, assert_close, check_argmax, bits16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -101,3 +106,69 @@ def test_fused_overflow_leaves_sequence_untouched(w):
     same(got, ref)
     assert int(got[4][-1]) == w.cap - 5
     assert int(got[5][0]) & cpa.EBIT["CAPACITY"]
+
+
+def oracle_fused(w, inp, ck, cv, L0, rows, mask=None, len0=None):
+    """The oracle's attention (past lengths L0) over the cache as it is before
+    the append, then its global append of rows [0, rows[b]) after len0 (L0 by
+    default) cached rows; the cache format follows ck's dtype."""
+    kv = "f16" if ck.dtype == torch.float16 else "bf16"
+    sel = (inp["n_real"] - 1).clamp(min=0)
+    ref, ref_sel = oracle_attn(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], ck, cv, w.P, L0,
+                               inp["n_real"], mask=mask, sel_row=sel)
+    k_np, v_np = bits16(ck).copy(), bits16(cv).copy()
+    length = (L0 if len0 is None else len0).numpy().astype(np.int64).copy()
+    over = O.kv_append_global(k_np, v_np, length, bf16_bits(inp["k"]), bf16_bits(inp["v"]), inp["cos"].numpy(),
+                              inp["sin"].numpy(), rows.numpy(), kv=kv)
+    return ref, ref_sel, k_np, v_np, length, over
+
+
+def check_against_oracle(cpa, w, got, inp, ck, cv, L0, rows, mask=None, len0=None):
+    out, sel, gk, gv, glen, err = got
+    ref, ref_sel, k_np, v_np, length, over = oracle_fused(w, inp, ck, cv, L0, rows, mask, len0)
+    assert_close(out, ref, w.name + "/fused out")
+    if (inp["n_real"] > 0).all():
+        check_argmax(sel, ref_sel, w.name + "/fused sel")
+    assert glen.cpu().numpy().tolist() == length.tolist()
+    gk16, gv16 = bits16(gk), bits16(gv)
+    for b in range(w.B):
+        n = int(length[b])
+        assert np.array_equal(gk16[b, :, :n], k_np[b, :, :n]), f"{w.name}: cache K of sequence {b}"
+        assert np.array_equal(gv16[b, :, :n], v_np[b, :, :n]), f"{w.name}: cache V of sequence {b}"
+    e = int(err[0])
+    assert bool(e & cpa.EBIT["CAPACITY"]) == bool(over), (e, over)
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fused_matches_oracle(w):
+    cpa = lib()
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    got = run(cpa, w, fused=True, alias=True)
+    check_against_oracle(cpa, w, got, inp, ck, cv, inp["past_len"], inp["n_real"])
+
+
+def test_fused_matches_oracle_explicit_mask_rows_and_overflow():
+    """The single-tile case with an explicit 512-window mask, the two-tile
+    case with n_rows != n_real and a sequence that overflows its cache."""
+    cpa = lib()
+    w = CASES[2]
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, 512, 1)
+    got = run(cpa, w, fused=True, alias=False, mask=mask)
+    check_against_oracle(cpa, w, got, inp, ck, cv, inp["past_len"], inp["n_real"], mask=mask)
+
+    w = CASES[0]
+    inp = make_chunk_inputs(w)
+    ck, cv = make_cache(w)
+    rows = torch.tensor([3, 40], dtype=torch.int32)
+    got = run(cpa, w, fused=True, alias=False, n_rows=rows)
+    check_against_oracle(cpa, w, got, inp, ck, cv, inp["past_len"], rows)
+
+    # the cache of the last sequence holds cap - 5 rows: its append overflows
+    # (the attention still reads past_len rows)
+    L = w.past_lens().clone()
+    L[-1] = w.cap - 5
+    got = run(cpa, w, fused=True, alias=False, len0=L)
+    check_against_oracle(cpa, w, got, inp, ck, cv, inp["past_len"], inp["n_real"], len0=L)

@@ -267,3 +267,88 @@ def test_page1_signature_counts():
     results = 2 * layers + 1
     assert args == int(g["args"][0]) and results == int(g["results"][0])
     assert int(g["select_row"][0]) == int(g["real"][0]) - 1
+
+
+# ------------------------------------------------------------------ selected-row argmax
+
+def test_select_argmax_hand_placed_maxima_and_ties():
+    """One row per case, maxima placed by hand: the pick is per row along the
+    last axis, in fp32 (two values 2^-20 apart, equal once rounded to bf16,
+    still order), and the lowest index wins a tie."""
+    rows = np.full((4, 12), -3.0, dtype=np.float32)
+    rows[0, 9] = 5.0                                   # a single maximum late in the row
+    rows[1, 2] = rows[1, 7] = 4.0                      # a tie: the lower index
+    rows[2, 4] = np.float32(1.0) + np.float32(2.0 ** -20)
+    rows[2, 3] = 1.0                                   # bf16 would round both to 1.0
+    rows[3, :] = 0.5                                   # every value equal: index 0
+    got = O.select_argmax(rows)
+    assert got.shape == (4,)
+    assert got.tolist() == [9, 2, 4, 0]
+    assert O.f32_to_bf16(rows[2, 3:5]).tolist()[0] == O.f32_to_bf16(rows[2, 3:5]).tolist()[1]
+    # a batch of rows against a per-row scan written out here
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((6, 40)).astype(np.float32)
+    x[:, 5] = x[:, 17] = x.max(axis=1) + 1.0
+    want = [min(j for j in range(40) if x[r, j] == x[r].max()) for r in range(6)]
+    assert O.select_argmax(x).tolist() == want == [5] * 6
+
+
+# ------------------------------------------------------------------ fp16 cache reading
+
+def test_f16_reading_at_position_zero_equals_bf16_reading():
+    """Tables at position 0 (cos 1, sin 0) leave every key unrotated, and
+    N(0,1) bf16 values convert to half exactly: the fp16-cache reading then
+    sees the same numbers as the bf16 one, so the outputs are equal."""
+    B, Hq, Hkv, C, D, P = 1, 4, 2, 6, 32, 9
+    q = bf16_bits(normal_bf16((B, Hq, C, D), 0, "pin/f16z_q"))
+    k = bf16_bits(normal_bf16((B, Hkv, C, D), 0, "pin/f16z_k"))
+    v = bf16_bits(normal_bf16((B, Hkv, C, D), 0, "pin/f16z_v"))
+    ck = bf16_bits(normal_bf16((B, Hkv, P, D), 0, "pin/f16z_ck"))
+    cv = bf16_bits(normal_bf16((B, Hkv, P, D), 0, "pin/f16z_cv"))
+    cos = np.ones((B, C, D), dtype=np.float32)
+    sin = np.zeros((B, C, D), dtype=np.float32)
+    a32, _ = O.chunk_prefill_attn(q, k, v, cos, sin, ck, cv, P, [7], [5])
+    a16, _ = O.chunk_prefill_attn(q, k, v, cos, sin, O.to_kv(ck, "f16"), O.to_kv(cv, "f16"), P, [7], [5],
+                                  kv="f16")
+    assert np.array_equal(a32, a16)
+
+
+def test_f16_reading_matches_library_sdpa_on_half_operands():
+    """General positions: the fp16-cache reading is fp64 softmax attention over
+    Q and the chunk keys rotated to half, the half cache rows and the chunk
+    values converted to half.  The half operands are formed here with torch's
+    own conversions from an fp64 complex rotation (a different route from the
+    oracle's fp32 arithmetic, so single half-ulp differences may appear) and
+    the attention by the library's SDPA with GQA and a boolean mask.  On these
+    seeded inputs both routes give the same half operands, so the outputs
+    agree to fp64 rounding; a bf16 rounding of Q or of the chunk keys in place
+    of half moves them by ~3e-3."""
+    B, Hq, Hkv, C, D, P, L, n = 1, 8, 2, 10, 64, 21, 17, 8
+    q = normal_bf16((B, Hq, C, D), 0, "pin/f16s_q")
+    k = normal_bf16((B, Hkv, C, D), 0, "pin/f16s_k")
+    v = normal_bf16((B, Hkv, C, D), 0, "pin/f16s_v")
+    ck = normal_bf16((B, Hkv, P, D), 0, "pin/f16s_ck").half()
+    cv = normal_bf16((B, Hkv, P, D), 0, "pin/f16s_cv").half()
+    cos, sin = rope_tables(L + np.arange(C)[None, :], D, 10000.0)
+    h16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    out, _ = O.chunk_prefill_attn(bf16_bits(q), bf16_bits(k), bf16_bits(v), cos.numpy(), sin.numpy(),
+                                  h16(ck), h16(cv), P, [L], [n], kv="f16")
+
+    def rot_half(x):
+        xf = x.double()
+        h = D // 2
+        c = cos.double()[:, None]
+        s = sin.double()[:, None]
+        z = torch.complex(xf[..., :h], xf[..., h:]) * torch.complex(c[..., :h], s[..., :h])
+        return torch.cat([z.real, z.imag], dim=-1).half().double()
+
+    keys = torch.cat([ck.double(), rot_half(k)], dim=2)
+    vals = torch.cat([cv.double(), v.half().double()], dim=2)
+    vis = torch.from_numpy(O.visible(L, n, C, P, 0, 1))
+    lib = F.scaled_dot_product_attention(rot_half(q), keys, vals, attn_mask=vis[None, None],
+                                         enable_gqa=True).numpy()
+    assert np.max(np.abs(out - lib)) < 1e-9
+    # and the half reading is not the bf16 one: rounding to half moved it
+    b16, _ = O.chunk_prefill_attn(bf16_bits(q), bf16_bits(k), bf16_bits(v), cos.numpy(), sin.numpy(),
+                                  bf16_bits(ck.bfloat16()), bf16_bits(cv.bfloat16()), P, [L], [n])
+    assert np.max(np.abs(b16 - out)) > 0
