@@ -455,6 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.w = pack16x2<F16>(x[8 * c8 + 6], x[8 * c8 + 7]);
         *reinterpret_cast<uint4*>(sP + (c8 / 8) * (kBM * 128) + sw128(row, c8 % 8)) = w;
       }
+      if (!p.mask) {
+        // dead V rows of this tile (cache slots past the length, chunk pad
+        // rows) are cleared once the tile has landed, before the P V product
+        int z0, z1;
+        dead_rows<BN>(p, tp, chunk, base, z0, z1);
+        if (z0 < z1) {
+          const int st = q % kStages;
+          if (!(ok = warp_all(mbar_wait(&bars->v_full[st], (q / kStages) & 1, abort)))) break;
+          zero_tile_rows<D>(sV + st * SM::kVBytes, BN, z0, z1, tid, 128);
+        }
+      }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full);

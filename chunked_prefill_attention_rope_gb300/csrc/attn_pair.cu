@@ -894,6 +894,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             }
           }
         }
+        if (!EXPLICIT && qi == 0) {
+          // this tile's dead V rows (cache slots past the length, chunk pad
+          // rows) are cleared once the tile has landed and before either P V
+          // product reads it (both wait for this warpgroup's P)
+          int z0, z1;
+          dead_rows<kBN>(p, tp, chunk, base, z0, z1);
+          if (z0 < z1) {
+            const int st = gt % NS;
+            if (!(ok = warp_all(mbar_wait(&bars->v_full[st], (gt / NS) & 1, abort)))) break;
+            zero_tile_rows<D>(sV + st * CF::kVBytes, kBN, z0, z1, row, 128);
+            fence_async_smem();
+          }
+        }
         const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
         tmem_st_wait();
         l_run = __fmaf_rn(l_run, factor, sum);

@@ -247,6 +247,18 @@ __global__ void __launch_bounds__(kDThreads, 2)
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
 
+    if (!EXPLICIT && !chunk) {
+      // dead V rows among this warp's keys (cache slots past the length) are
+      // cleared before its P V product reads them: P is zero there, but 0
+      // times a non-finite value is not
+      const int z0 = max(L - base, key0), z1 = min(min(p.P - base, kDBN), key0 + 16);
+      if (z0 < z1) {
+        zero_tile_rows<D>(smem + CF::kV + st * CF::kTile, kDBN, z0, z1, lane, 32);
+        fence_async_smem();  // the ring slot is refilled by TMA later
+        __syncwarp();
+      }
+    }
+
     // S = Q K^T for 16 keys: two n-blocks of 8 keys
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll

@@ -104,6 +104,33 @@ struct RowSpan {
   }
 };
 
+// Rows of key tile [base, base + BN) that the implicit mask never shows to any
+// query row but that the tile copy fills from memory: cache slots in [L, P)
+// (dead rows: nothing promises their bytes) and chunk pad rows in [n, C).
+// Rows at or past P (or C) arrive as zeros from the copy.  Returns [z0, z1)
+// relative to the tile (empty when z0 >= z1).  P is exactly zero for these
+// keys, but 0 times a non-finite value is not zero, so the kernels clear
+// these rows of the V tile before the P V product.
+template <int BN>
+__device__ __forceinline__ void dead_rows(const AttnParams& p, const TilePlan& tp, bool chunk, int base, int& z0,
+                                          int& z1) {
+  z0 = max((chunk ? tp.n : tp.L) - base, 0);
+  z1 = min((chunk ? p.C : p.P) - base, BN);
+}
+
+// Zero rows [r0, r1) of a 128-byte-swizzled tile stored as D/64 blocks of
+// `rows` rows x 128 bytes (the swizzle only permutes 16-byte chunks inside a
+// row), by `nthreads` threads of which this is `tid`.
+template <int D>
+__device__ __forceinline__ void zero_tile_rows(uint8_t* tile, int rows, int r0, int r1, int tid, int nthreads) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  const int n = (r1 - r0) * kChunks;
+  for (int k = tid; k < n; k += nthreads) {
+    const int r = r0 + k / kChunks, c = k % kChunks;
+    *reinterpret_cast<uint4*>(tile + (c / 8) * (rows * 128) + r * 128 + (c % 8) * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // Fused append, device side: write rotated key chunk pair (lo, hi) and the
 // value chunks of chunk row i of (b, kv head h) into the cache, if the
 // sequence has room (len + n <= cap) and i < n.
