@@ -27,7 +27,7 @@ __all__ = [
     "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
     "decode_step", "chunk_prefill_attn_append",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
-    "attn_workspace_size", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
+    "attn_workspace_size", "attn_workspace_size_mask", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
     "tail_plan", "TAIL_SCALAR", "TAIL_PADDED", "TAIL_AUTO", "TAIL_FORCE_SCALAR", "TAIL_FORCE_PADDED",
 ]
 
@@ -89,6 +89,8 @@ def load_library():
     lib.cpa_chunk_prefill_attn_append.argtypes = [ctypes.POINTER(_AttnArgs), vp, vp]
     lib.cpa_attn_workspace_size.argtypes = [i32] * 6
     lib.cpa_attn_workspace_size.restype = sz
+    lib.cpa_attn_workspace_size_mask.argtypes = [i32] * 6
+    lib.cpa_attn_workspace_size_mask.restype = sz
     lib.cpa_kv_append.argtypes = [ctypes.POINTER(_Cache), vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, sz, vp, vp]
     lib.cpa_cache_scratch_size.argtypes = [ctypes.POINTER(_Cache), i32, i32, i32, i32]
     lib.cpa_cache_scratch_size.restype = sz
@@ -160,6 +162,11 @@ def attn_workspace_size(B, Hq, Hkv, D, C, P) -> int:
     return int(load_library().cpa_attn_workspace_size(B, Hq, Hkv, D, C, P))
 
 
+def attn_workspace_size_mask(B, Hq, Hkv, D, C, P) -> int:
+    """Workspace for a call with an explicit mask (room for the mask's bit copy)."""
+    return int(load_library().cpa_attn_workspace_size_mask(B, Hq, Hkv, D, C, P))
+
+
 def cache_scratch_size(cache: KVCache, C: int) -> int:
     s = cache.struct()
     return int(load_library().cpa_cache_scratch_size(ctypes.byref(s), cache.B, cache.Hkv, cache.D, C))
@@ -187,7 +194,7 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
     _need(out, "out", torch.bfloat16, (B, Hq, C, D))
     if out_sel is None and want_sel:
         out_sel = torch.empty((B, Hq * D), dtype=torch.float32, device=q.device)
-    need = lib.cpa_attn_workspace_size(B, Hq, Hkv, D, C, P)
+    need = (lib.cpa_attn_workspace_size_mask if mask is not None else lib.cpa_attn_workspace_size)(B, Hq, Hkv, D, C, P)
     if workspace is None and need > 0 and alloc_workspace:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if err is None:

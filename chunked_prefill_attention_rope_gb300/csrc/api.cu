@@ -135,8 +135,13 @@ SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int 
   return w;
 }
 
-size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
-  if (g.path == kPathPair) return pair_workspace(B, Hq, Hkv, D, C, g.teams).total;
+// Bytes of workspace for these sizes; `mask_bits`: with room for the two-tile
+// path's bit copy of an explicit mask (the other paths need no more for it).
+size_t workspace_bytes(const Geometry& g, int B, int Hq, int Hkv, int D, int C, int P, bool mask_bits = false) {
+  if (g.path == kPathPair) {
+    const PairWorkspace w = pair_workspace(B, Hq, Hkv, D, C, P, g.teams);
+    return mask_bits ? w.total_bits : w.total;
+  }
   return single_workspace(g, B, Hq, Hkv, D, C).total;
 }
 
@@ -190,7 +195,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   if (static_cast<long long>(a->B) * a->Hq * a->C * a->D > (1LL << 40)) return CPA_ERR_SHAPE;
 
   const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, a->sm_budget);
-  const size_t need = workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C);
+  const size_t need = workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
   if (need > 0 && (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)))
     return CPA_ERR_WORKSPACE;
 
@@ -218,6 +223,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.cluster = g.cluster ? 1 : 0;
   const double scale = a->scale > 0.f ? static_cast<double>(a->scale) : 1.0 / sqrt(static_cast<double>(a->D));
   p.sl2 = static_cast<float>(scale * 1.4426950408889634);
+  p.inv_scale = static_cast<float>(1.0 / scale);
   p.q = static_cast<const uint16_t*>(a->q);
   p.cos = a->cos;
   p.sin = a->sin;
@@ -255,9 +261,18 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     p.teams = t.teams;
     p.ctas = t.ctas;
     uint8_t* w = static_cast<uint8_t*>(a->workspace);
-    const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, a->D, a->C, t);
+    const PairWorkspace L = pair_workspace(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, t);
     p.ustart = reinterpret_cast<int32_t*>(w + L.ustart);
-    p.perm = t.perm && !a->mask && p.sink <= 0 ? 1 : 0;
+    // the plan depends on the shapes and the visited tiles only, whatever the
+    // mask form, so that both forms of one mask split the work alike
+    p.perm = t.perm ? 1 : 0;
+    p.ntiles = (a->C + 127) / 128 + (a->P + 127) / 128;
+    if (a->mask) {
+      p.tcls = w + L.tcls;
+      p.hull = reinterpret_cast<int4*>(w + L.hull);
+      // the mask's bit copy when the caller's workspace has room for it
+      p.mbits = a->workspace_bytes >= L.total_bits ? reinterpret_cast<uint4*>(w + L.mbits) : nullptr;
+    }
     p.uorder = reinterpret_cast<int32_t*>(w + L.uorder);
     p.upos = reinterpret_cast<int32_t*>(w + L.upos);
     p.tlo = reinterpret_cast<int32_t*>(w + L.tlo);
@@ -326,7 +341,7 @@ size_t attn_workspace_need(const cpa_attn_args* a) {
       a->Hq / a->Hkv > 128 || !valid_d(a->D) || a->sm_budget < 0)
     return 0;
   const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, a->sm_budget);
-  return workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C);
+  return workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
 }
 
 }  // namespace cpa
@@ -350,7 +365,12 @@ cpa_status cpa_chunk_prefill_attn_append(const cpa_attn_args* args, const int32_
 
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P) {
   if (B < 1 || Hq < 1 || Hkv < 1 || C < 1 || P < 0 || Hq % Hkv || Hq / Hkv > 128 || !valid_d(D)) return 0;
-  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, Hkv, D, C);
+  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, Hkv, D, C, P);
+}
+
+size_t cpa_attn_workspace_size_mask(int B, int Hq, int Hkv, int D, int C, int P) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || C < 1 || P < 0 || Hq % Hkv || Hq / Hkv > 128 || !valid_d(D)) return 0;
+  return workspace_bytes(geometry(B, Hq, Hkv, D, C, P), B, Hq, Hkv, D, C, P, true);
 }
 
 size_t cpa_cache_scratch_size(const cpa_cache* cache, int B, int Hkv, int D, int C) {

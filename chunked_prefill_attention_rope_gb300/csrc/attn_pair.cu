@@ -75,12 +75,10 @@ struct PairCfg {
   static constexpr int kBars = kV + kStages * kVBytes;
   static constexpr int kOCol = 2 * kBN;  // O0 at [256, 256 + D), O1 at [256 + D, 256 + 2D)
   static_assert(kOCol + 2 * D <= 512, "TMEM columns");
-  // a 4 KB staging tile per softmax warp (32 rows x 32 fp32 columns): the
-  // epilogue's coalesced stores and, with an explicit mask, the mask's
-  // coalesced loads; then (explicit mask only) each warp's 32 mask-row indices
+  // a 4 KB staging tile per softmax warp (32 rows x 32 fp32 columns) for the
+  // epilogue's coalesced stores
   static constexpr int kStage = kBars + 256;
-  static constexpr int kMaskRows = kStage + 8 * 32 * 32 * 4;
-  static constexpr int kMaskEnd = kMaskRows + 8 * 32 * 4;
+  static constexpr int kStageEnd = kStage + 8 * 32 * 32 * 4;
 };
 
 struct __align__(8) PairBars {
@@ -91,12 +89,12 @@ struct __align__(8) PairBars {
   int abort;
 };
 
-template <int D, bool EXPLICIT>
+template <int D>
 constexpr int pair_smem_bytes() {
   static_assert(sizeof(PairBars) <= 256, "barrier block");
-  return (EXPLICIT ? PairCfg<D>::kMaskEnd : PairCfg<D>::kMaskRows) + 1024;
+  return PairCfg<D>::kStageEnd + 1024;
 }
-static_assert(pair_smem_bytes<128, true>() <= 227 * 1024, "shared memory");
+static_assert(pair_smem_bytes<128>() <= 227 * 1024, "shared memory");
 
 struct Unit {
   int b, kvh, pair;
@@ -115,11 +113,28 @@ __device__ __forceinline__ Block block_of(const AttnParams& p, int g) {
   return x;
 }
 
+__device__ __forceinline__ int block_index(const AttnParams& p, const Block& x) {
+  return (x.b * p.Hkv + x.kvh) * p.nblk + x.blk;
+}
+
 // Live key tiles of all rows of a block: the tiles its members walk together.
+// Explicit mask: the chunk tiles and the past tiles from the first to the
+// last one holding a visible entry for some row of the block (mask_scan_kernel
+// and the plan find them); for a mask that writes out the implicit one these
+// are exactly the implicit mask's tile intervals, so both forms visit the same
+// tiles and split the work alike.
 __device__ __forceinline__ TilePlan block_plan(const AttnParams& p, const Block& x) {
   const int i_min = x.blk * p.team * 2 * p.R;
   const int i_max = min(i_min + p.team * 2 * p.R, p.C) - 1;
-  return plan_whole<kBN>(p, x.b, i_min, i_max);
+  TilePlan t = plan_whole<kBN>(p, x.b, i_min, i_max);
+  if (p.mask) {
+    const int4 h = p.hull[block_index(p, x)];
+    t.cb = h.x;
+    t.ce = h.y;
+    t.pb = h.z;
+    t.pe = h.w;
+  }
+  return t;
 }
 
 __device__ __forceinline__ Unit unit_of(const AttnParams& p, int u) {
@@ -335,6 +350,115 @@ __device__ void plan_units(const AttnParams& p) {
   if (threadIdx.x == 0) p.tlo[teams + 1] = whole ? 1 : 0;  // whole blocks: no unit is cut
 }
 
+// Classes of a key tile of one block under an explicit mask.
+enum : uint8_t {
+  kTileDead = 0,     // no entry above -1e29 (every key masked for every row)
+  kTileBinary = 1,   // every entry 0 or at most -1e29: the pages' 0 / -1e30 form
+  kTileGeneral = 2,  // some entry is a finite bias (or not a number)
+};
+
+constexpr int kScanThreads = 256;
+constexpr int kScanBatch = 8;  // mask rows a warp has in flight
+
+// Explicit mask pre-pass of the two-tile path.  One CTA per (block, key
+// tile) reads that tile's entries of every mask row of the block once: a
+// warp takes one row's 128 keys per load, four consecutive keys per lane.
+// It records the tile's class and, when p.mbits is set, each row's
+// visibility bits: word j, bit l holds key 4 l + j of the tile, set when the
+// entry is exactly 0 (the attention tests bit (q % 4, q / 4) for key q).
+// Keys past the row's end (P or C) read as masked.
+__global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParams p) {
+  grid_launch_dependents();
+  grid_dependency_wait();  // the mask may come from the work before this call
+  const int T = p.ntiles;
+  const int g = blockIdx.x / T, t = blockIdx.x % T;
+  const Block x = block_of(p, g);
+  const int Tc = (p.C + kBN - 1) / kBN;
+  const bool chunk = t < Tc;
+  const int base = (chunk ? t : t - Tc) * kBN;
+  const int lim = (chunk ? p.C : p.P) - base;
+  const size_t moff = chunk ? static_cast<size_t>(p.P) + base : static_cast<size_t>(base);
+  const size_t stride = static_cast<size_t>(p.P) + p.C;
+  const int i0 = x.blk * p.team * 2 * p.R;
+  const int ni = min(i0 + p.team * 2 * p.R, p.C) - i0;  // chunk rows of the block
+  const int rows = p.G * ni;                             // mask rows: heads x chunk rows
+  const bool vec = (p.P % 4 == 0) && (p.C % 4 == 0);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int k0 = 4 * lane;
+  bool live = false, general = false;
+  for (int r0 = warp * 32; r0 < rows; r0 += kScanThreads) {
+    uint4 mine = make_uint4(0u, 0u, 0u, 0u);  // bits of row r0 + lane
+    for (int j0 = 0; j0 < 32 && r0 + j0 < rows; j0 += kScanBatch) {
+      float v[kScanBatch][4];
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) {
+        const int r = r0 + j0 + u;
+        v[u][0] = v[u][1] = v[u][2] = v[u][3] = -1e30f;
+        if (r < rows) {
+          const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
+          const float* row = p.mask + (static_cast<size_t>(x.b * p.Hq + h) * p.C + i) * stride + moff;
+          if (vec) {
+            if (k0 < lim) {
+              const float4 f = __ldg(reinterpret_cast<const float4*>(row + k0));
+              v[u][0] = f.x;
+              v[u][1] = f.y;
+              v[u][2] = f.z;
+              v[u][3] = f.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (k0 + e < lim) v[u][e] = __ldg(row + k0 + e);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float m = v[u][e];
+          live |= m > -1e29f;
+          general |= !(m == 0.f || m <= -1e29f);
+          w[e] = __ballot_sync(0xffffffffu, m == 0.f);
+        }
+        if (lane == j0 + u) mine = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    if (p.mbits && r0 + lane < rows) {
+      const int r = r0 + lane;
+      const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
+      p.mbits[(static_cast<size_t>(x.b * p.Hq + h) * T + t) * p.C + i] = mine;
+    }
+  }
+  live = __syncthreads_or(live);
+  general = __syncthreads_or(general);
+  if (threadIdx.x == 0) p.tcls[blockIdx.x] = !live ? kTileDead : (general ? kTileGeneral : kTileBinary);
+}
+
+// Explicit mask: each block's visited tiles (first to last non-dead chunk
+// tile, and likewise for the past tiles) from the scan's classes, by one CTA
+// of kPrepThreads threads, before the plan prices the blocks.
+__device__ void explicit_hulls(const AttnParams& p) {
+  const int T = p.ntiles, Tc = (p.C + kBN - 1) / kBN;
+  for (int g = threadIdx.x; g < p.blocks; g += kPrepThreads) {
+    const uint8_t* c = p.tcls + static_cast<size_t>(g) * T;
+    int cb = 0, ce = 0, pb = Tc, pe = Tc;
+    for (int t = 0; t < Tc; ++t)
+      if (c[t] != kTileDead) {
+        if (ce == 0) cb = t;
+        ce = t + 1;
+      }
+    for (int t = Tc; t < T; ++t)
+      if (c[t] != kTileDead) {
+        if (pe == Tc) pb = t;
+        pe = t + 1;
+      }
+    p.hull[g] = make_int4(cb, ce, pb, pe);
+  }
+  __syncthreads();  // the hulls, read by other threads of this CTA
+}
+
 // CTA 0 plans (plan_units); the others rotate the chunk's queries and
 // keys into the workspace.  An item is one (sequence, chunk row, chunk pair)
 // and up to four heads of the combined list [query heads, key heads]: the
@@ -345,6 +469,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
   grid_launch_dependents();
   grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
   if (blockIdx.x == 0) {  // the first CTA to start plans, alongside the rotations
+    if (p.mask) explicit_hulls(p);
     plan_units(p);
     return;
   }
@@ -402,32 +527,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
 }
 
 // Explicit mask values of keys [k0, k0 + 32) of a tile for this thread's row
-// (`mp`: the row at the tile's first key, or null), one value at a time, -1e30
-// at or past `lim`: the path for P or C not a multiple of 4.
-__device__ __forceinline__ void load_mask32(float (&mv)[32], const float* mp, int k0, int lim) {
+// (`mp`: the row at the tile's first key, or null), -1e30 at or past `lim`.
+// `vec`: P and C are multiples of 4, so each row starts 16-byte aligned and no
+// 16-byte vector straddles `lim`.
+__device__ __forceinline__ void load_mask32(float (&mv)[32], const float* mp, int k0, int lim, bool vec) {
+  if (vec) {
 #pragma unroll
-  for (int q = 0; q < 32; ++q) mv[q] = (mp && k0 + q < lim) ? __ldg(mp + k0 + q) : -1e30f;
-}
-
-// Explicit mask values of keys [k0, k0 + 32) of a tile for the 32 rows of one
-// warp, read coalesced: eight loads of 16 bytes per lane, lane l taking keys
-// k0 + 4 (l % 8) of rows 4 k + l / 8, so that four rows share one load
-// instruction.  `rows` holds the warp's mask-row indices (-1: none) in the
-// order row % 4, row / 4; `moff` is the tile's first key in the mask row and
-// keys at or past `lim` read -1e30.  Needs P and C multiples of 4, so that no
-// vector straddles `lim`.
-__device__ __forceinline__ void fetch_mask32(float4 (&v)[8], const float* mask, size_t stride, const int* rows,
-                                             int lane, size_t moff, int k0, int lim) {
-  const int4 ra = reinterpret_cast<const int4*>(rows)[(lane >> 3) * 2];
-  const int4 rb = reinterpret_cast<const int4*>(rows)[(lane >> 3) * 2 + 1];
-  const int ridx[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-  const int col = lane & 7;
-  const bool in = k0 + 4 * col < lim;
+    for (int k = 0; k < 8; ++k) {
+      float4 v = make_float4(-1e30f, -1e30f, -1e30f, -1e30f);
+      if (mp && k0 + 4 * k < lim) v = __ldg(reinterpret_cast<const float4*>(mp + k0 + 4 * k));
+      mv[4 * k] = v.x;
+      mv[4 * k + 1] = v.y;
+      mv[4 * k + 2] = v.z;
+      mv[4 * k + 3] = v.w;
+    }
+  } else {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    v[k] = make_float4(-1e30f, -1e30f, -1e30f, -1e30f);
-    if (in && ridx[k] >= 0)
-      v[k] = __ldg(reinterpret_cast<const float4*>(mask + static_cast<size_t>(ridx[k]) * stride + moff + k0 + 4 * col));
+    for (int q = 0; q < 32; ++q) mv[q] = (mp && k0 + q < lim) ? __ldg(mp + k0 + q) : -1e30f;
   }
 }
 
@@ -438,28 +554,6 @@ __device__ __forceinline__ void mask_span(const AttnParams& p, const TilePlan& t
   const int base = (chunk ? t : t - tp.Tc) * kBN;
   lim = chunk ? p.C - base : p.P - base;
   moff = chunk ? static_cast<size_t>(p.P) + base : static_cast<size_t>(base);
-}
-
-// The values fetch_mask32 read, handed to the lane that owns each row through
-// the warp's staging tile (16-byte slots XOR-swizzled by row, so neither the
-// stores nor the loads have bank conflicts).
-__device__ __forceinline__ void deal_mask32(float (&mv)[32], const float4 (&v)[8], float4* stg, int lane) {
-  const int col = lane & 7;
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int r = 4 * k + (lane >> 3);
-    stg[r * 8 + (col ^ (r & 7))] = v[k];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 x = stg[lane * 8 + (k ^ (lane & 7))];
-    mv[4 * k] = x.x;
-    mv[4 * k + 1] = x.y;
-    mv[4 * k + 2] = x.z;
-    mv[4 * k + 3] = x.w;
-  }
 }
 
 // SINK: the implicit mask also keeps pinned sink slots visible (a separate
@@ -681,7 +775,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t o_col = tmem + lanes + CF::kOCol + qi * D;
     const float sl2 = p.sl2;
     float4* mstage = reinterpret_cast<float4*>(smem + CF::kStage) + warp * 32 * 8;  // this warp's staging tile
-    int* mrows = reinterpret_cast<int*>(smem + CF::kMaskRows) + warp * 32;
     int g = 0, seg = 0;
     bool ok = true;
     int unit, a, e;
@@ -700,17 +793,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const bool mask_vec = (p.P % 4 == 0) && (p.C % 4 == 0);
       const size_t mstride = static_cast<size_t>(p.P + p.C);
       const float* mrow = nullptr;
-      if (EXPLICIT) {
-        const int ridx = valid ? (x.b * p.Hq + h) * p.C + i : -1;
-        if (valid) mrow = p.mask + static_cast<size_t>(ridx) * mstride;
-        __syncwarp();
-        mrows[(lane & 3) * 8 + (lane >> 2)] = ridx;
-        __syncwarp();
-      }
+      if (EXPLICIT && valid) mrow = p.mask + (static_cast<size_t>(x.b * p.Hq + h) * p.C + i) * mstride;
       float m_run = kMaskedLog2, l_run = 0.f;
       const int n = e - a;
-      float4 fq[2][8];          // explicit mask: two chunks in flight
-      bool mask_ahead = false;  // fq already holds this tile's first two chunks
       for (int jj = 0; jj < n; ++jj) {
         const int gt = g + jj;
         const int t = tp.index(a + jj);
@@ -718,27 +803,54 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         const int base = (chunk ? t : t - tp.Tc) * kBN;
         int lo, hi, sk;
         span.tile(chunk, base, lo, hi, sk);
-        const float* mp = nullptr;
-        int lim = 0;
-        size_t moff = 0;
+        // Explicit mask: the tile's class (one for every row of the block)
+        // and, for a tile of 0 and masked entries, this row's visibility bits,
+        // loaded before the wait on S.  Without a bit copy such tiles take the
+        // fp32 values, which give the same result.
+        int cls = kTileBinary;
+        uint4 vb = make_uint4(0u, 0u, 0u, 0u);
         if (EXPLICIT) {
-          mask_span(p, tp, t, moff, lim);
-          if (mrow) mp = mrow + moff;
+          cls = p.tcls[static_cast<size_t>(block_index(p, bx)) * p.ntiles + t];
+          if (cls == kTileBinary && !p.mbits) cls = kTileGeneral;
+          if (cls == kTileBinary && valid)
+            vb = p.mbits[(static_cast<size_t>(x.b * p.Hq + h) * p.ntiles + t) * p.C + i];
         }
         if (!(ok = warp_all(mbar_wait(&bars->s_full[qi], gt & 1, abort)))) break;
         tc_fence_after();
         if (jj + 1 == n) mbar_arrive(&bars->q_free[qi]);  // last S = Q K of the segment is done
 
-        // Scores of this row.  Implicit mask: one batch of TMEM loads, masked
-        // keys set to -inf (they give exactly 0 below).  Explicit mask: the row
-        // max of scale*s + mask (in log2 units), chunk by chunk.
+        if (EXPLICIT && cls == kTileGeneral) {
+          // Finite biases: s + bias / scale is written back over S (masked
+          // keys -inf), so that the exponentials below form
+          // 2^(scale*log2e*s + log2e*bias - m); an entry of 0 leaves s as it is.
+          size_t moff;
+          int lim;
+          mask_span(p, tp, t, moff, lim);
+          const float* mp = mrow ? mrow + moff : nullptr;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            float mc[32];
+            load_mask32(mc, mp, 32 * c, lim, mask_vec);
+            uint32_t r[32];
+            tmem_ld32(s_col + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              r[q] = __float_as_uint(mc[q] > -1e29f ? __fmaf_rn(mc[q], p.inv_scale, __uint_as_float(r[q])) : -INFINITY);
+            tmem_st32(s_col + 32 * c, r);
+          }
+          tmem_st_wait();
+        }
+
+        // Scores of this row: one batch of TMEM loads, masked keys set to -inf
+        // (they give exactly 0 below).  The implicit mask masks by the row's
+        // visible intervals, an explicit 0 / masked tile by its bits.
         float sc[kBN];
-        float m_tile;
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(s_col + 32 * c, sc + 32 * c);
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
         if (!EXPLICIT) {
-#pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(s_col + 32 * c, sc + 32 * c);
-#pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) tmem_ld_waitf(sc + 32 * c);
           if (__any_sync(0xffffffffu, lo > 0 || hi < kBN)) {
             if (!SINK || !__any_sync(0xffffffffu, sk > 0)) {
 #pragma unroll
@@ -754,74 +866,23 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
               }
             }
           }
-          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+        } else if (cls != kTileGeneral) {
+          if (__any_sync(0xffffffffu, (vb.x & vb.y & vb.z & vb.w) != 0xffffffffu)) {
+            const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};  // key q: word q % 4, bit q / 4
 #pragma unroll
-          for (int q = 0; q < kBN; q += 8) {
-            m0 = fmax3(m0, sc[q], sc[q + 1]);
-            m1 = fmax3(m1, sc[q + 2], sc[q + 3]);
-            m2 = fmax3(m2, sc[q + 4], sc[q + 5]);
-            m3 = fmax3(m3, sc[q + 6], sc[q + 7]);
+            for (int q = 0; q < kBN; ++q) sc[q] = ((vw[q & 3] >> (q >> 2)) & 1u) ? sc[q] : -INFINITY;
           }
-          const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-          m_tile = (mt == -INFINITY) ? kMaskedLog2 : __fmul_rn(mt, sl2);
-        } else {
-          float mt = -INFINITY;
-          // t = scale*log2e*s + log2e*mask, chunk by chunk (the mask fetched
-          // two chunks ahead and dealt out), written back over S for the
-          // exponentials below; the row max of t on the way.
-          if (mask_vec && !mask_ahead) {
-            fetch_mask32(fq[0], p.mask, mstride, mrows, lane, moff, 0, lim);
-            fetch_mask32(fq[1], p.mask, mstride, mrows, lane, moff, 32, lim);
-          }
-          float mt0 = -INFINITY, mt1 = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            float mc[32];
-            if (mask_vec) {
-              deal_mask32(mc, fq[c & 1], mstage, lane);
-              if (c + 2 < kBN / 32) fetch_mask32(fq[c & 1], p.mask, mstride, mrows, lane, moff, 32 * (c + 2), lim);
-            } else {
-              load_mask32(mc, mp, 32 * c, lim);
-            }
-            uint32_t r[32];
-            tmem_ld32(s_col + 32 * c, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-              const float2 lo2 = ffma2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])),
-                                       make_float2(sl2, sl2),
-                                       fmul2(make_float2(mc[q], mc[q + 1]), make_float2(kLog2e, kLog2e)));
-              const float2 hi2 = ffma2(make_float2(__uint_as_float(r[q + 2]), __uint_as_float(r[q + 3])),
-                                       make_float2(sl2, sl2),
-                                       fmul2(make_float2(mc[q + 2], mc[q + 3]), make_float2(kLog2e, kLog2e)));
-              mt0 = fmax3(mt0, lo2.x, lo2.y);
-              mt1 = fmax3(mt1, hi2.x, hi2.y);
-              r[q] = __float_as_uint(lo2.x);
-              r[q + 1] = __float_as_uint(lo2.y);
-              r[q + 2] = __float_as_uint(hi2.x);
-              r[q + 3] = __float_as_uint(hi2.y);
-            }
-            tmem_st32(s_col + 32 * c, r);
-          }
-          tmem_st_wait();
-          mt = fmaxf(mt0, mt1);
-          // the next tile's first two chunks load (and its last two move to
-          // L2) while this tile's exponentials run and its next S is made
-          mask_ahead = mask_vec && jj + 1 < n;
-          if (mask_ahead) {
-            size_t moff1;
-            int lim1;
-            mask_span(p, tp, tp.index(a + jj + 1), moff1, lim1);
-            fetch_mask32(fq[0], p.mask, mstride, mrows, lane, moff1, 0, lim1);
-            fetch_mask32(fq[1], p.mask, mstride, mrows, lane, moff1, 32, lim1);
-            if (mrow) {
-#pragma unroll
-              for (int k = 64; k < kBN; k += 32)
-                if (k < lim1) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(mrow + moff1 + k)));
-            }
-          }
-          m_tile = mt;
         }
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kBN; q += 8) {
+          m0 = fmax3(m0, sc[q], sc[q + 1]);
+          m1 = fmax3(m1, sc[q + 2], sc[q + 3]);
+          m2 = fmax3(m2, sc[q + 4], sc[q + 5]);
+          m3 = fmax3(m3, sc[q + 6], sc[q + 7]);
+        }
+        const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        const float m_tile = (mt == -INFINITY) ? kMaskedLog2 : __fmul_rn(mt, sl2);
         const float m_new = fmaxf(m_run, m_tile);
         const bool rescale = m_new > m_run + 8.f;
         float factor = 1.f;
@@ -855,44 +916,17 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           }
           tmem_st16(s_col + 16 * c, w);
         };
-        if (!EXPLICIT) {
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            float* pv = sc + 32 * c;
-            const float nm = live ? -m_run : -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 32; q += 2) {
-              const float2 y = ffma2(make_float2(pv[q], pv[q + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-              pv[q] = fast_exp2(y.x);
-              pv[q + 1] = fast_exp2(y.y);
-            }
-            emit(pv, c);
-          }
-        } else {
-          // P = 2^(t - m) from the t written above, two chunks per
-          // tensor-memory round trip (chunk c + 1's P lands over chunk c's t,
-          // already in registers)
+        for (int c = 0; c < kBN / 32; ++c) {
+          float* pv = sc + 32 * c;
           const float nm = live ? -m_run : -INFINITY;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32; c += 2) {
-            uint32_t ra[32], rb[32];
-            tmem_ld32(s_col + 32 * c, ra);
-            tmem_ld32(s_col + 32 * (c + 1), rb);
-            tmem_ld_wait(ra);
-            tmem_ld_wait(rb);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t (&r)[32] = h ? rb : ra;
-              float pv[32];
-#pragma unroll
-              for (int q = 0; q < 32; q += 2) {
-                const float2 y = fadd2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])), make_float2(nm, nm));
-                pv[q] = fast_exp2(y.x);
-                pv[q + 1] = fast_exp2(y.y);
-              }
-              emit(pv, c + h);
-            }
+          for (int q = 0; q < 32; q += 2) {
+            const float2 y = ffma2(make_float2(pv[q], pv[q + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+            pv[q] = fast_exp2(y.x);
+            pv[q + 1] = fast_exp2(y.y);
           }
+          emit(pv, c);
         }
         if (!EXPLICIT && qi == 0) {
           // this tile's dead V rows (cache slots past the length, chunk pad
@@ -1163,7 +1197,7 @@ PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms) {
   return t;
 }
 
-PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t) {
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, int P, const PairTeams& t) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const int ctas = t.ctas;
   PairWorkspace w;
@@ -1178,13 +1212,18 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTea
   w.q_rot = off; off += al(static_cast<size_t>(B) * Hq * C * D * 2);
   w.k_rot = off; off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
   w.v_cvt = off; off += al(static_cast<size_t>(B) * Hkv * C * D * 2);  // fp16 cache: chunk values in half
+  const size_t T = static_cast<size_t>((C + kBN - 1) / kBN + (P + kBN - 1) / kBN);
+  w.tcls = off; off += al(static_cast<size_t>(t.blocks) * T);                  // explicit mask: tile classes
+  w.hull = off; off += al(static_cast<size_t>(t.blocks) * 16);                 // explicit mask: tile hulls
   w.total = off;
+  w.mbits = off; off += al(static_cast<size_t>(B) * Hq * T * C * 16);          // explicit mask: bit copy
+  w.total_bits = off;
   return w;
 }
 
 template <int D, bool EXPLICIT, bool SINK, bool F16, bool PERM>
 static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  constexpr int smem = pair_smem_bytes<D, EXPLICIT>();
+  constexpr int smem = pair_smem_bytes<D>();
   auto kern = attn_pair_kernel<D, EXPLICIT, SINK, F16, PERM>;
   static SmemAttr smem_attr;
   if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), smem); e != cudaSuccess) return e;
@@ -1192,7 +1231,13 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
                           (p.D / 16);
   const int rope_blocks =
       static_cast<int>(max(1LL, min(static_cast<long long>(65535) * 4, (items + kPrepThreads - 1) / kPrepThreads)));
-  cudaError_t e = launch_dependent(prep_kernel, dim3(rope_blocks + 1), dim3(kPrepThreads), 0, stream, p);
+  cudaError_t e;
+  if (EXPLICIT) {  // classify the mask's tiles before the plan reads them
+    e = launch_dependent(mask_scan_kernel, dim3(static_cast<unsigned>(p.blocks) * p.ntiles), dim3(kScanThreads), 0,
+                         stream, p);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_dependent(prep_kernel, dim3(rope_blocks + 1), dim3(kPrepThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_dependent(kern, dim3(p.ctas), dim3(kThreadsPair), smem, stream, maps[0], maps[1], maps[2], maps[3],
                        maps[4], p);
@@ -1201,12 +1246,19 @@ static cudaError_t launch_pair_t(const CUtensorMap* maps, const AttnParams& p, c
                           stream, p);
 }
 
+// The walk (planned order or index order) follows the shapes alone, so the
+// explicit and implicit forms of one mask take the same plan.
+template <int D, bool F16, bool EXPLICIT, bool SINK>
+static cudaError_t launch_pair_w(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
+  if (p.perm) return launch_pair_t<D, EXPLICIT, SINK, F16, true>(maps, p, stream);
+  return launch_pair_t<D, EXPLICIT, SINK, F16, false>(maps, p, stream);
+}
+
 template <int D, bool F16>
 static cudaError_t launch_pair_d(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
-  if (p.mask) return launch_pair_t<D, true, false, F16, false>(maps, p, stream);
-  if (p.sink > 0) return launch_pair_t<D, false, true, F16, false>(maps, p, stream);
-  if (p.perm) return launch_pair_t<D, false, false, F16, true>(maps, p, stream);
-  return launch_pair_t<D, false, false, F16, false>(maps, p, stream);
+  if (p.mask) return launch_pair_w<D, F16, true, false>(maps, p, stream);
+  if (p.sink > 0) return launch_pair_w<D, F16, false, true>(maps, p, stream);
+  return launch_pair_w<D, F16, false, false>(maps, p, stream);
 }
 
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {

@@ -31,7 +31,9 @@ struct SmemAttr {
 };
 
 // Workspace bytes the attention call described by `a` needs, sized for its
-// own sm_budget (0 for sizes the call would reject).
+// own sm_budget (0 for sizes the call would reject).  This is the minimum: an
+// explicit mask on the two-tile path runs faster with more (see
+// cpa_attn_workspace_size_mask).
 size_t attn_workspace_need(const cpa_attn_args* a);
 
 // Launch `kern` as a programmatic dependent of the grid before it on the
@@ -103,6 +105,15 @@ struct AttnParams {
   int64_t app_sb, app_sh, app_ss;  // cache strides in elements
   int32_t* app_len;
   int app_cap;
+  // Explicit mask on the two-tile path: mask_scan_kernel classifies every
+  // (block, key tile) and the plan visits the tiles between each block's
+  // first and last tile holding a visible entry (the implicit mask's tile
+  // intervals when the mask is the implicit one written out).
+  float inv_scale;   // 1 / softmax scale: a finite bias b enters as s + b / scale
+  int ntiles;        // key tiles per block: chunk tiles, then past tiles
+  uint8_t* tcls;     // [blocks * ntiles] tile classes (kTileDead / kTileBinary / kTileGeneral)
+  int4* hull;        // [blocks] visited tiles: chunk [x, y), past [z, w) in the tile index space
+  uint4* mbits;      // [B, Hq, ntiles, C] visibility bits of each row and tile, or null
 };
 
 
@@ -113,9 +124,10 @@ struct PairTeams {
 };
 PairTeams pair_teams(int B, int Hkv, int nq, int P, int C, int num_sms);
 struct PairWorkspace {
-  size_t ustart, uorder, upos, tlo, part_o, part_lse, ptag, q_rot, k_rot, v_cvt, total;
+  size_t ustart, uorder, upos, tlo, part_o, part_lse, ptag, q_rot, k_rot, v_cvt, tcls, hull, total;
+  size_t mbits, total_bits;  // the explicit mask's bit copy goes last: [total, total_bits)
 };
-PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, const PairTeams& t);
+PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, int P, const PairTeams& t);
 // maps for the pair path: cache K, cache V, rotated chunk K, chunk V, rotated Q
 // (dims {D, C, Hq, B}, box {64, R, G, 1}).
 cudaError_t launch_attn_pair5(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream);

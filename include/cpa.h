@@ -192,6 +192,18 @@ cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream);
  * sizes (0 when the step runs without split-KV partials). */
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P);
 
+/* Bytes of workspace for a call with an explicit mask at these sizes: at
+ * least cpa_attn_workspace_size(...).  On the two-tile path (D = 64 or 128
+ * with more than 128 packed query rows per kv head) a pre-pass reads the
+ * fp32 mask once and classifies every key tile; with this much workspace it
+ * also keeps a one-bit copy of each row's entries that are exactly 0 (1/32
+ * of the mask's bytes), so that tiles holding only 0 and masked entries
+ * ([P1, Change]: 0 = attend, -1e30 = masked) are never read in fp32 again.
+ * With only cpa_attn_workspace_size(...) bytes the attention re-reads the
+ * fp32 values of the tiles it visits.  The results are the same bits either
+ * way. */
+size_t cpa_attn_workspace_size_mask(int B, int Hq, int Hkv, int D, int C, int P);
+
 /*
  * cpa_chunk_prefill_attn for callers that cannot allocate device memory.  The
  * pages have no counterpart: this exists for callers with no way to obtain a

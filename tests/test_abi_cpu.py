@@ -26,7 +26,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     _, so = lib
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for name in names:
         assert hasattr(so, name), name
 
@@ -44,6 +44,16 @@ def test_workspace_sizes(lib):
     assert so.cpa_attn_workspace_size(1, 3, 2, 128, 1, 10) == 0
     assert so.cpa_attn_workspace_size(1, 4, 1, 96, 1, 10) == 0
     assert so.cpa_attn_workspace_size(64, 32, 8, 128, 1, 32768) > 0
+    # an explicit mask on the two-tile path: room for a bit per mask entry on
+    # top (16 bytes per row and 128-key tile); other paths need nothing more
+    B, Hq, Hkv, D, C, P = 16, 32, 8, 128, 128, 4096
+    plain = so.cpa_attn_workspace_size(B, Hq, Hkv, D, C, P)
+    masked = so.cpa_attn_workspace_size_mask(B, Hq, Hkv, D, C, P)
+    tiles = (C + 127) // 128 + (P + 127) // 128
+    assert masked - plain >= B * Hq * C * tiles * 16
+    assert masked - plain < B * Hq * C * tiles * 16 + 256
+    assert so.cpa_attn_workspace_size_mask(1, 4, 1, 256, 64, 800) == so.cpa_attn_workspace_size(1, 4, 1, 256, 64, 800)
+    assert so.cpa_attn_workspace_size_mask(1, 3, 2, 128, 1, 10) == 0
 
 
 def _args(cpa, **kw):

@@ -16,7 +16,7 @@ import torch
 
 import oracle as O
 from synth import Workload, make_chunk_inputs, make_cache, normal_bf16, rope_tables, bf16_bits, uniform_int
-from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks, bits16, two_tile_path,
+from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks, bits16,
                      assert_explicit_matches)
 
 pytestmark = pytest.mark.gpu
@@ -69,7 +69,7 @@ def test_f16_cache_attention_matches_oracle(w):
     mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, w.window, w.causal)
     out_e, _ = run_gpu(cpa, inp, ck, cv, w.P, mask=mask)
     assert_close(out_e, ref, w.name + "/explicit")
-    assert_explicit_matches(out_e, out, two_tile_path(w.D, w.Hq, w.Hkv, w.C), w.name)
+    assert_explicit_matches(out_e, out, w.name)
 
 
 @pytest.mark.parametrize("D,Hkv", [(64, 1), (128, 4), (256, 2)])

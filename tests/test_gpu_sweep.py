@@ -17,7 +17,7 @@ import pytest
 import torch
 
 from synth import Workload, make_chunk_inputs, make_cache
-from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks, two_tile_path,
+from harness import (lib, assert_close, check_argmax, oracle_attn, explicit_masks,
                      assert_explicit_matches)
 
 pytestmark = pytest.mark.gpu
@@ -74,7 +74,7 @@ def test_sweep_matches_oracle(w):
     mask = explicit_masks(inp["past_len"].numpy(), inp["n_real"].numpy(), w.C, w.P, w.Hq, w.window, w.causal)
     out_e, _, _ = run(cpa, inp, ck, cv, w, mask=mask)
     assert_close(out_e, ref, w.name + "/explicit")
-    assert_explicit_matches(out_e, out, two_tile_path(w.D, w.Hq, w.Hkv, w.C), w.name)
+    assert_explicit_matches(out_e, out, w.name)
 
 
 @pytest.mark.parametrize("w", CASES[::3], ids=lambda w: w.name)
