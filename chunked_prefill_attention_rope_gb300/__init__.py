@@ -17,6 +17,7 @@ stream.  The entry points mirror include/cpa.h:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -24,7 +25,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CpaError", "KVCache", "load_library", "lib_path", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
+    "CpaError", "KVCache", "load_library", "lib_path", "using_library", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
     "decode_step", "chunk_prefill_attn_append",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
     "attn_workspace_size", "attn_workspace_size_mask", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
@@ -35,7 +36,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 GLOBAL, SLIDING = 0, 1
 TAIL_SCALAR, TAIL_PADDED = 0, 1
 TAIL_AUTO, TAIL_FORCE_SCALAR, TAIL_FORCE_PADDED = 0, 1, 2
-EBIT = dict(CAPACITY=1, PAST_GT_SPAN=2, NREAL_GT_C=4, SLIDING_N=8, SNAPSHOT=16, TIMEOUT=32)
+EBIT = dict(CAPACITY=1, PAST_GT_SPAN=2, NREAL_GT_C=4, SLIDING_N=8, SNAPSHOT=16, TIMEOUT=32, BOUNDS=64)
 
 
 class CpaError(RuntimeError):
@@ -65,19 +66,37 @@ class _AttnArgs(ctypes.Structure):
                 ("sm_budget", ctypes.c_int)]
 
 
-_LIB = None
+_LIBS = {}
+_VARIANT = "default"
+_LIB_FILES = {"default": "libcpa.so", "checked": "libcpa_checked.so"}
 
 
-def lib_path() -> str:
-    return os.path.join(_HERE, "libcpa.so")
+def lib_path(variant: Optional[str] = None) -> str:
+    return os.path.join(_HERE, _LIB_FILES[variant or _VARIANT])
 
 
-def load_library():
-    """Load libcpa.so (raises if it is missing: run build() first)."""
-    global _LIB
-    if _LIB is not None:
-        return _LIB
-    path = lib_path()
+@contextlib.contextmanager
+def using_library(variant: str):
+    """Route the calls inside the block to one build of the library:
+    "default" (libcpa.so) or "checked" (libcpa_checked.so, the bounds-checked
+    build with its test hooks)."""
+    global _VARIANT
+    if variant not in _LIB_FILES:
+        raise ValueError(f"unknown library variant {variant!r}")
+    old = _VARIANT
+    _VARIANT = variant
+    try:
+        yield load_library(variant)
+    finally:
+        _VARIANT = old
+
+
+def load_library(variant: Optional[str] = None):
+    """Load the library (raises if it is missing: run build() first)."""
+    v = variant or _VARIANT
+    if v in _LIBS:
+        return _LIBS[v]
+    path = lib_path(v)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with "
                            "chunked_prefill_attention_rope_gb300.build.build()")
@@ -104,7 +123,10 @@ def load_library():
               "cpa_chunk_prefill_attn_append", "cpa_kv_append",
               "cpa_kv_snapshot_padded_append", "cpa_kv_rollback_padded_append", "cpa_tail_plan"):
         getattr(lib, f).restype = i32
-    _LIB = lib
+    if v == "checked":
+        lib.cpa_test_drop_tile.argtypes = [i32]
+        lib.cpa_test_drop_tile.restype = None
+    _LIBS[v] = lib
     return lib
 
 

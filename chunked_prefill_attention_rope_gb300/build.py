@@ -1,8 +1,16 @@
-"""Build libcpa.so (the C-ABI library) in-tree for sm_103a with nvcc.
+"""Build the C-ABI library in-tree for sm_103a with nvcc.
 
-Each .cu file compiles in parallel into _build/, then one link step writes
-libcpa.so next to this file.  Rebuilds only when a source or header is newer
-than the library.
+Two variants of the same sources:
+  libcpa.so          the library;
+  libcpa_checked.so  a checked build for tests (-DCPA_BOUNDS_CHECK: every
+                     global index the kernels compute is range-checked and an
+                     index out of range sets CPA_EBIT_BOUNDS instead of being
+                     used; -DCPA_TEST_HOOKS: a short in-kernel wait limit and a
+                     test hook that withholds one tile copy, so that a bounded
+                     wait can be made to run out).
+Every .cu file of both variants compiles in parallel into _build/<variant>/,
+then one link step per variant writes the library next to this file.  A
+variant is rebuilt only when a source or header is newer than its library.
 """
 from __future__ import annotations
 
@@ -22,6 +30,14 @@ LIB = os.path.join(HERE, "libcpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{os.path.join(ROOT, 'include')}"]
+VARIANTS = {
+    "default": ("libcpa.so", []),
+    "checked": ("libcpa_checked.so", ["-DCPA_BOUNDS_CHECK", "-DCPA_TEST_HOOKS"]),
+}
+
+
+def lib_file(variant: str = "default") -> str:
+    return os.path.join(HERE, VARIANTS[variant][0])
 
 
 def nvcc() -> str:
@@ -40,36 +56,45 @@ def _inputs():
         [os.path.join(ROOT, "include", "cpa.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(variant: str = "default") -> bool:
+    lib = lib_file(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra=(), variants=("default", "checked")) -> str:
+    """Build the requested variants (all by default); returns the path of libcpa.so."""
+    todo = [v for v in variants if force or not up_to_date(v)]
+    if not todo:
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(job):
+        variant, src = job
+        out_dir = os.path.join(BUILD, variant)
+        os.makedirs(out_dir, exist_ok=True)
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
+        cmd = [cc, *ARCH, *FLAGS, *VARIANTS[variant][1], *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} ({variant}):\n{r.stdout}\n{r.stderr}")
         if verbose and (r.stdout or r.stderr):
             sys.stderr.write(r.stdout + r.stderr)
-        return obj
+        return variant, obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp"
-    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(v, s) for v in todo for s in _sources()]
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for v in todo:
+        lib = lib_file(v)
+        tmp = lib + ".tmp"
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *[o for vv, o in objs if vv == v]],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed ({v}):\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

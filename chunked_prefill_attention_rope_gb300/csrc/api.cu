@@ -8,6 +8,9 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#ifdef CPA_TEST_HOOKS
+#include "../../include/cpa_test.h"
+#endif
 
 using namespace cpa;
 
@@ -48,6 +51,15 @@ bool make_map(CUtensorMap* m, const void* base, int D, int rows, int heads, int 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checked build's test hook: the key tile whose copy each two-tile CTA
+// withholds (-1: none); the regular build never withholds one.
+#ifdef CPA_TEST_HOOKS
+std::atomic<int> g_test_drop_tile{-1};
+int test_drop_tile() { return g_test_drop_tile.load(std::memory_order_relaxed); }
+#else
+int test_drop_tile() { return -1; }
+#endif
 
 // SM count of the current device, queried once per device (devices 0-63).
 int num_sms() {
@@ -160,8 +172,16 @@ cpa_status check_cache(const cpa_cache* c, int D) {
   return CPA_OK;
 }
 
-CacheView view_of(const cpa_cache* c) {
+// Elements spanned by a [B, Hkv, cap, D] view with these strides.
+long long view_extent(const cpa_cache* c, int B, int Hkv, int D) {
+  return static_cast<long long>(B - 1) * c->stride_b + static_cast<long long>(Hkv - 1) * c->stride_h +
+         static_cast<long long>(c->cap - 1) * c->stride_s + D;
+}
+
+CacheView view_of(const cpa_cache* c, int B, int Hkv, int D, int32_t* err) {
   CacheView v;
+  v.extent = view_extent(c, B, Hkv, D);
+  v.err = err;
   v.k = static_cast<uint16_t*>(c->k);
   v.v = static_cast<uint16_t*>(c->v);
   v.sb = c->stride_b;
@@ -241,7 +261,9 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.err = a->err;
   p.k_new = static_cast<const uint16_t*>(a->k_new);
   p.v_new = static_cast<const uint16_t*>(a->v_new);
+  p.test_drop_tile = test_drop_tile();
   if (app_n && g.path != kPathDecode) {
+    p.n_app = view_extent(c, a->B, a->Hkv, a->D);
     p.app_n = app_n;
     p.app_k = static_cast<uint16_t*>(c->k);
     p.app_v = static_cast<uint16_t*>(c->v);
@@ -278,6 +300,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     p.tlo = reinterpret_cast<int32_t*>(w + L.tlo);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
     p.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+    p.n_part = static_cast<long long>(t.ctas) * 2 * 256 * a->D;
     p.ptag = reinterpret_cast<int32_t*>(w + L.ptag);
     p.q_rot = reinterpret_cast<uint16_t*>(w + L.q_rot);
     p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
@@ -296,6 +319,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   if (g.splits > 1 && !g.cluster) {
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
     p.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+    p.n_part = static_cast<long long>(g.splits) * a->B * a->Hq * a->C * a->D;
   }
   if (g.path == kPathSingle) {
     // raw Q rows (box {64, R, G, 1}); chunk keys from the rotated copy
@@ -312,9 +336,11 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     // attention (one token: the separate append kernels after the attention)
     const cudaError_t e =
         g.path == kPathDecode
-            ? launch_global_append(view_of(c), ChunkView{static_cast<const uint16_t*>(a->k_new),
-                                                         static_cast<const uint16_t*>(a->v_new), a->cos, a->sin,
-                                                         app_n},
+            ? launch_global_append(view_of(c, a->B, a->Hkv, a->D, a->err),
+                                   ChunkView{static_cast<const uint16_t*>(a->k_new),
+                                             static_cast<const uint16_t*>(a->v_new), a->cos, a->sin, app_n,
+                                             static_cast<long long>(a->B) * a->Hkv * a->C * a->D,
+                                             static_cast<long long>(a->B) * a->C * a->D},
                                    a->B, a->Hkv, a->D, a->C, a->err, stream)
             : launch_fused_append_len(p, stream);
     if (e != cudaSuccess) return CPA_ERR_CUDA;
@@ -384,8 +410,9 @@ cpa_status cpa_kv_append(const cpa_cache* cache, const void* k_new, const void* 
   cpa_status st = chunk_check(k_new, v_new, cos, sin, n_rows, B, Hkv, D, C, err);
   if (st != CPA_OK) return st;
   if ((st = check_cache(cache, D)) != CPA_OK) return st;
-  const CacheView cv = view_of(cache);
-  ChunkView x{static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), cos, sin, n_rows};
+  const CacheView cv = view_of(cache, B, Hkv, D, err);
+  ChunkView x{static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), cos, sin, n_rows,
+              static_cast<long long>(B) * Hkv * C * D, static_cast<long long>(B) * C * D};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (cache->kind == CPA_CACHE_GLOBAL) {
@@ -410,7 +437,7 @@ cpa_status cpa_kv_snapshot_padded_append(const cpa_cache* cache, const int32_t* 
   if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
   const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
   if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
-  return launch_snapshot(view_of(cache), n_real, B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
+  return launch_snapshot(view_of(cache, B, Hkv, D, err), n_real, B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CPA_OK
              : CPA_ERR_CUDA;
@@ -427,7 +454,7 @@ cpa_status cpa_kv_rollback_padded_append(const cpa_cache* cache, int B, int Hkv,
   if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
   const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
   if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
-  return launch_rollback(view_of(cache), B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
+  return launch_rollback(view_of(cache, B, Hkv, D, err), B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CPA_OK
              : CPA_ERR_CUDA;
@@ -475,5 +502,9 @@ const char* cpa_status_str(cpa_status s) {
 }
 
 const char* cpa_version(void) { return "cpa 0.1 (sm_103a)"; }
+
+#ifdef CPA_TEST_HOOKS
+void cpa_test_drop_tile(int tile) { g_test_drop_tile.store(tile, std::memory_order_relaxed); }
+#endif
 
 }  // extern "C"

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int item = (threadIdx.x - 64) + 128 * u;
       const int il = item / (D / 16), kc = item % (D / 16);
       const int ri = qt * p.R + il;
-      if (item < q_items && ri < p.C) {
+      if (item < q_items && ri < p.C && in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) {
         const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
         const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
         qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (item >= q_items || qt * R + il >= p.C) continue;
           if (it0 > 0) {
             const int ri = qt * R + il;
+            if (!in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) continue;
             const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
             const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
             qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
@@ -324,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch_lo = W > 0 ? max(0, i - W + 1) : 0;
     const int ch_hi = p.causal ? min(tp.n, i + 1) : (W > 0 ? min(tp.n, i + W) : tp.n);
     const bool mask_vec = (p.P % 4 == 0) && (p.C % 4 == 0);
-    const float* mrow = (p.mask && valid)
-                            ? p.mask + ((static_cast<size_t>(b) * p.Hq + h) * p.C + i) * static_cast<size_t>(p.P + p.C)
+    const long long mrow_off = ((static_cast<long long>(b) * p.Hq + h) * p.C + i) * (static_cast<long long>(p.P) + p.C);
+    const float* mrow = (p.mask && valid && in_bounds(mrow_off, static_cast<long long>(p.P) + p.C, n_mask(p), p.err))
+                            ? p.mask + mrow_off
                             : nullptr;
 
     float m_run = kMaskedLog2, l_run = 0.f;
@@ -509,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(stg + row * SM::kStg + 32 * c + e) = v;
         }
       }
-      if (valid && p.part_o) p.part_lse[static_cast<size_t>(split) * p.B * p.Hq * p.C + orow_me] = lse_me;
+      if (valid && p.part_o)
+        st_chk(p.part_lse, static_cast<long long>(split) * p.B * p.Hq * p.C + orow_me, p.n_part / D, lse_me, p.err);
       named_bar_sync(1, 128);
       // This warp's own 32 rows, whole rows with lanes across D: bf16 output
       // (one split) or fp32 partials.  Row indices come from the table, four
@@ -523,6 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long orow = tab_row[r];
         if (orow < 0) continue;
         const float* src = stg + r * SM::kStg;
+        if (!in_bounds(static_cast<long long>(p.part_o ? part_base + orow : orow) * D, D,
+                       p.part_o ? p.n_part : n_qo(p), p.err))
+          continue;
         if (p.part_o) {
           float* dst = p.part_o + (part_base + static_cast<size_t>(orow)) * D;
 #pragma unroll
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 v = *reinterpret_cast<const float4*>(src + e);
             *reinterpret_cast<uint2*>(dst + e) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
           }
-          if (p.out_sel && tab_i[r] == sel) {
+          if (p.out_sel && tab_i[r] == sel && in_bounds(static_cast<long long>(tab_bh[r]) * D, D, n_sel(p), p.err)) {
             float* sd = p.out_sel + static_cast<size_t>(tab_bh[r]) * D;
 #pragma unroll
             for (int e = 4 * lane; e < D; e += 128)
@@ -629,8 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (lane >= NCH) continue;
+        if (!in_bounds(orow * D, D, n_qo(p), p.err)) continue;
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        const bool is_sel = p.out_sel && tab_i[r] == sel;
+        const bool is_sel = p.out_sel && tab_i[r] == sel && in_bounds(static_cast<long long>(tab_bh[r]) * D, D, n_sel(p), p.err);
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
           const int e = lane + 32 * q;
@@ -667,6 +674,9 @@ __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
     const long long r = it / HP;  // row of [B, Hkv, C]
     const int i = static_cast<int>(r % p.C);
     const int b = static_cast<int>(r / p.C / p.Hkv);
+    if (!in_bounds(r * D, D, n_chunk(p), p.err) ||
+        !in_bounds((static_cast<long long>(b) * p.C + i) * D, D, n_tab(p), p.err))
+      continue;
     const uint16_t* src = p.k_new + r * D;
     uint4 lo = __ldg(reinterpret_cast<const uint4*>(src + kc * 8));
     uint4 hi = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
@@ -709,6 +719,10 @@ __global__ void combine_kernel(const AttnParams p) {
   const int b = bh / p.Hq;
   const int h = bh % p.Hq;
   const size_t stride = static_cast<size_t>(rows);
+  if (!in_bounds((static_cast<long long>(p.splits - 1) * stride + row) * p.D, p.D, p.n_part, p.err) ||
+      !in_bounds(static_cast<long long>(row) * p.D, p.D, n_qo(p), p.err) ||
+      !in_bounds((static_cast<long long>(b) * p.Hq + h) * p.D, p.D, n_sel(p), p.err))
+    return;
   // the splits' log2-sum-exps spread over the lanes, then the warp's maximum
   float lmax = -INFINITY;
   for (int s = lane; s < p.splits; s += 32) lmax = fmaxf(lmax, p.part_lse[s * stride + row]);

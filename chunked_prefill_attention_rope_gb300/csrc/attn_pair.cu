@@ -128,7 +128,8 @@ __device__ __forceinline__ TilePlan block_plan(const AttnParams& p, const Block&
   const int i_max = min(i_min + p.team * 2 * p.R, p.C) - 1;
   TilePlan t = plan_whole<kBN>(p, x.b, i_min, i_max);
   if (p.mask) {
-    const int4 h = p.hull[block_index(p, x)];
+    const int gi = block_index(p, x);
+    const int4 h = in_bounds(gi, 1, p.blocks, p.err) ? p.hull[gi] : make_int4(0, 0, t.Tc, t.Tc);
     t.cb = h.x;
     t.ce = h.y;
     t.pb = h.z;
@@ -201,7 +202,9 @@ struct SegWalk {
       const Pos aa = lo > t0 ? lo : t0;
       const Pos ee = hi < s1 ? hi : s1;
       if (ee <= aa) continue;
-      const Block x = block_of(*pp, PERM ? pp->uorder[cur] : cur);
+      const int gb = PERM ? pp->uorder[cur] : cur;
+      if (!in_bounds(gb, 1, NB, pp->err)) continue;
+      const Block x = block_of(*pp, gb);
       const int pair = x.blk * pp->team + member;
       if (pair >= pp->pairs) continue;
       blk = x;
@@ -339,7 +342,7 @@ __device__ void plan_units(const AttnParams& p) {
   }
   for (int k = threadIdx.x; k < NB; k += kPrepThreads) {
     p.uorder[k] = order[k];
-    p.upos[order[k]] = k;
+    st_chk(p.upos, order[k], NB, k, p.err);
   }
   prefix_costs(NB, [&](int k) { return cost[order[k]]; }, p.ustart);
   __syncthreads();  // ustart, written by other threads of this CTA
@@ -396,7 +399,9 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParam
         v[u][0] = v[u][1] = v[u][2] = v[u][3] = -1e30f;
         if (r < rows) {
           const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
-          const float* row = p.mask + (static_cast<size_t>(x.b * p.Hq + h) * p.C + i) * stride + moff;
+          const long long ro = (static_cast<long long>(x.b * p.Hq + h) * p.C + i) * stride + moff;
+          const float* row = p.mask + ro;
+          if (!in_bounds(ro, lim, n_mask(p), p.err)) continue;
           if (vec) {
             if (k0 < lim) {
               const float4 f = __ldg(reinterpret_cast<const float4*>(row + k0));
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParam
     if (p.mbits && r0 + lane < rows) {
       const int r = r0 + lane;
       const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
-      p.mbits[(static_cast<size_t>(x.b * p.Hq + h) * T + t) * p.C + i] = mine;
+      st_chk(p.mbits, (static_cast<long long>(x.b * p.Hq + h) * T + t) * p.C + i, n_bits(p), mine, p.err);
     }
   }
   live = __syncthreads_or(live);
@@ -488,6 +493,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
     const int b = static_cast<int>(t / groups);
     const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
     const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
+    if (!in_bounds((static_cast<long long>(b) * p.C + i) * D, D, n_tab(p), p.err)) continue;
     const RopeTab tab = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
     uint4 lo[kPrepHeads], hi[kPrepHeads];
     size_t off[kPrepHeads];
@@ -499,6 +505,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
       off[u] = is_q ? ((static_cast<size_t>(b) * p.Hq + hh) * p.C + i) * D
                     : ((static_cast<size_t>(b) * p.Hkv + (hh - p.Hq)) * p.C + i) * D;
       const uint16_t* src = (is_q ? p.q : p.k_new) + off[u];
+      if (!in_bounds(static_cast<long long>(off[u]), D, is_q ? n_qo(p) : n_chunk(p), p.err)) {
+        off[u] = ~size_t(0);  // skipped below
+        lo[u] = hi[u] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       lo[u] = __ldg(reinterpret_cast<const uint4*>(src + kc * 8));
       hi[u] = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
     }
@@ -506,6 +517,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
     for (int u = 0; u < kPrepHeads; ++u) {
       const int hh = grp * kPrepHeads + u;
       if (hh >= HH) break;
+      if (kChecked && off[u] == ~size_t(0)) continue;
       if (p.f16) {
         rope_apply<true>(lo[u], hi[u], tab);
         if (hh >= p.Hq) {  // an fp16 cache: the chunk's values in half too
@@ -529,8 +541,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
 // Explicit mask values of keys [k0, k0 + 32) of a tile for this thread's row
 // (`mp`: the row at the tile's first key, or null), -1e30 at or past `lim`.
 // `vec`: P and C are multiples of 4, so each row starts 16-byte aligned and no
-// 16-byte vector straddles `lim`.
-__device__ __forceinline__ void load_mask32(float (&mv)[32], const float* mp, int k0, int lim, bool vec) {
+// 16-byte vector straddles `lim`.  Checked builds: `mo` is mp's element
+// offset in the mask of `mn` elements.
+__device__ __forceinline__ void load_mask32(float (&mv)[32], const float* mp, int k0, int lim, bool vec,
+                                            long long mo, long long mn, int32_t* err) {
+  if (mp && k0 < lim && !in_bounds(mo + k0, min(32, lim - k0), mn, err)) mp = nullptr;
   if (vec) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -591,8 +606,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
-    p.ptag[2 * cta] = -1;  // no partial result of this call yet
-    p.ptag[2 * cta + 1] = -1;
+    st_chk(p.ptag, 2 * cta, 2LL * p.ctas, -1, p.err);  // no partial result of this call yet
+    st_chk(p.ptag, 2 * cta + 1, 2LL * p.ctas, -1, p.err);
     if (cta == 0) {
       for (int b = 0; b < p.B; ++b) {
         if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
@@ -636,6 +651,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int j = a; j < e; ++j, ++g) {
           const int st = g % NS;
           if (!(ok = mbar_wait(&bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
+          // checked build's test hook: no copy for this tile, so that the
+          // consumer's bounded wait for it runs out
+          if (kTestHooks && g == p.test_drop_tile) continue;
           const int t = tp.index(j);
           const bool chunk = t < tp.Tc;
           const int base = (chunk ? t : t - tp.Tc) * kBN;
@@ -810,10 +828,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         int cls = kTileBinary;
         uint4 vb = make_uint4(0u, 0u, 0u, 0u);
         if (EXPLICIT) {
-          cls = p.tcls[static_cast<size_t>(block_index(p, bx)) * p.ntiles + t];
+          cls = ld_chk(p.tcls, static_cast<long long>(block_index(p, bx)) * p.ntiles + t,
+                       static_cast<long long>(p.blocks) * p.ntiles, p.err);
           if (cls == kTileBinary && !p.mbits) cls = kTileGeneral;
           if (cls == kTileBinary && valid)
-            vb = p.mbits[(static_cast<size_t>(x.b * p.Hq + h) * p.ntiles + t) * p.C + i];
+            vb = ld_chk(p.mbits, (static_cast<long long>(x.b * p.Hq + h) * p.ntiles + t) * p.C + i, n_bits(p), p.err);
         }
         if (!(ok = warp_all(mbar_wait(&bars->s_full[qi], gt & 1, abort)))) break;
         tc_fence_after();
@@ -827,10 +846,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           int lim;
           mask_span(p, tp, t, moff, lim);
           const float* mp = mrow ? mrow + moff : nullptr;
+          const long long mo = mrow ? static_cast<long long>(mrow - p.mask) + static_cast<long long>(moff) : 0;
 #pragma unroll 1
           for (int c = 0; c < kBN / 32; ++c) {
             float mc[32];
-            load_mask32(mc, mp, 32 * c, lim, mask_vec);
+            load_mask32(mc, mp, 32 * c, lim, mask_vec, mo, n_mask(p), p.err);
             uint32_t r[32];
             tmem_ld32(s_col + 32 * c, r);
             tmem_ld_wait(r);
@@ -960,7 +980,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // only a CTA's first and last segments can be partial: slots 0 and 1
       const int which = seg == 0 ? 0 : 1;
       const size_t slot = (static_cast<size_t>(cta) * 2 + which) * kUnitRows + qi * 128 + row;
-      if (!whole && qi == 0 && row == 0) p.ptag[2 * cta + which] = unit;
+      if (!whole && qi == 0 && row == 0) st_chk(p.ptag, 2 * cta + which, 2LL * p.ctas, unit, p.err);
       // Each 32-column chunk of the warp's 32 rows goes through the staging
       // tile (16-byte slots XOR-swizzled by row, conflict-free both ways) so
       // that the global stores are row-contiguous runs: 128 bytes per row for
@@ -986,7 +1006,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int rr = 4 * j + (lane >> 3), k = lane & 7;
-            st_global_hint(reinterpret_cast<float4*>(base + rr * D + 4 * k), mstage[rr * 8 + (k ^ (rr & 7))], keep);
+            if (in_bounds(static_cast<long long>(base - p.part_o) + rr * D + 4 * k, 4, p.n_part, p.err))
+              st_global_hint(reinterpret_cast<float4*>(base + rr * D + 4 * k), mstage[rr * 8 + (k ^ (rr & 7))], keep);
           }
         } else {
           uint4* st4 = reinterpret_cast<uint4*>(mstage);
@@ -1006,9 +1027,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             const bool ok_r = __shfl_sync(0xffffffffu, valid, rr);
             const unsigned long long orr = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(orow), rr);
             const uint4 wv = st4[rr * 4 + (k ^ ((rr >> 1) & 3))];
-            if (ok_r) *reinterpret_cast<uint4*>(p.out + orr * D + 32 * c + 8 * k) = wv;
+            if (ok_r) st16_chk(p.out, static_cast<long long>(orr) * D + 32 * c + 8 * k, n_qo(p), wv, p.err);
           }
-          if (p.out_sel && valid && i == sel) {
+          if (p.out_sel && valid && i == sel &&
+              in_bounds((static_cast<long long>(x.b) * p.Hq + h) * D + 32 * c, 32, n_sel(p), p.err)) {
             float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h) * D + 32 * c;
 #pragma unroll
             for (int q = 0; q < 32; q += 4)
@@ -1016,7 +1038,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           }
         }
       }
-      if (valid && !whole) p.part_lse[slot] = empty ? -INFINITY : m_run + __log2f(l_run);
+      if (valid && !whole) st_chk(p.part_lse, slot, p.n_part / D, empty ? -INFINITY : m_run + __log2f(l_run), p.err);
       g += n;
       ++seg;
     }
@@ -1062,7 +1084,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) fused_append_len(p, b);
   if (warp == 0) {
     const int gnat = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
-    const int gblk = PERM ? p.upos[gnat] : gnat;  // the block's place in the walk order
+    int gblk = PERM ? p.upos[gnat] : gnat;  // the block's place in the walk order
+    if (!in_bounds(gblk, 1, p.blocks, p.err)) gblk = 0;
     const int member = x.pair % p.team;
     const long long s0 = p.ustart[gblk], s1 = p.ustart[gblk + 1];
     const long long T = p.ustart[p.blocks];
@@ -1081,7 +1104,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
         int slot = -1;
         if (t <= t_last) {
           const int c = t * p.team + member;
-          const int tag0 = p.ptag[2 * c], tag1 = p.ptag[2 * c + 1];
+          const int tag0 = ld_chk(p.ptag, 2LL * c, 2LL * p.ctas, p.err);
+          const int tag1 = ld_chk(p.ptag, 2LL * c + 1, 2LL * p.ctas, p.err);
           slot = tag0 == unit ? 2 * c : (tag1 == unit ? 2 * c + 1 : -1);
         }
         const unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
@@ -1127,7 +1151,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
 #pragma unroll
         for (int k = 0; k < kMergePieceBatch; ++k) {
           ls[u][k] = -INFINITY;
-          if (live[u] && k0 + k < np) {
+          if (live[u] && k0 + k < np &&
+              in_bounds((static_cast<long long>(piece_slot[k0 + k]) * kUnitRows + r[u]) * D, D, p.n_part, p.err)) {
             const size_t sidx = static_cast<size_t>(piece_slot[k0 + k]) * kUnitRows + r[u];
             ls[u][k] = p.part_lse[sidx];
             if constexpr (V == 4)  // the last read of these rows: let L2 drop them first
@@ -1164,12 +1189,14 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
     for (int u = 0; u < kMergeRowBatch; ++u) {
       if (!live[u]) continue;
       const size_t orow = (static_cast<size_t>(x.b) * p.Hq + h[u]) * p.C + i[u];
+      if (!in_bounds(static_cast<long long>(orow) * D, D, n_qo(p), p.err)) continue;
+      const bool sel_ok = in_bounds((static_cast<long long>(x.b) * p.Hq + h[u]) * D, D, n_sel(p), p.err);
       const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
 #pragma unroll
       for (int q = 0; q < V; q += 2) {
         const float o0 = acc[u][q] * inv, o1 = acc[u][q + 1] * inv;
         *reinterpret_cast<uint32_t*>(p.out + orow * D + lane * V + q) = pack_bf16x2(o0, o1);
-        if (p.out_sel && i[u] == sel) {
+        if (p.out_sel && i[u] == sel && sel_ok) {
           float* sd = p.out_sel + (static_cast<size_t>(x.b) * p.Hq + h[u]) * D + lane * V + q;
           sd[0] = o0;
           sd[1] = o1;

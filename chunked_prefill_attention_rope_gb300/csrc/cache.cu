@@ -22,8 +22,14 @@ struct Hdr {
   int32_t v[8];
 };
 
-__device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ void st16(uint16_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+// 16-byte chunk i (element index) of a buffer of n elements; checked builds
+// range-check it (see common.cuh).
+__device__ __forceinline__ uint4 ld16(const uint16_t* base, size_t i, long long n, int32_t* err) {
+  return ld16_chk(base, static_cast<long long>(i), n, err);
+}
+__device__ __forceinline__ void st16(uint16_t* base, size_t i, long long n, uint4 v, int32_t* err) {
+  st16_chk(base, static_cast<long long>(i), n, v, err);
+}
 
 __device__ __forceinline__ size_t crow(const CacheView& c, int b, int h, int s) {
   return static_cast<size_t>(b) * c.sb + static_cast<size_t>(h) * c.sh + static_cast<size_t>(s) * c.ss;
@@ -34,11 +40,12 @@ __device__ __forceinline__ size_t crow(const CacheView& c, int b, int h, int s) 
 __device__ __forceinline__ void put_new_row(const CacheView& c, const ChunkView& x, int b, int h, int i,
                                             int dst, int kc, int Hkv, int D, int C) {
   const size_t src = ((static_cast<size_t>(b) * Hkv + h) * C + i) * D;
-  uint4 lo = ld16(x.k + src + kc * 8);
-  uint4 hi = ld16(x.k + src + D / 2 + kc * 8);
+  if (!in_bounds((static_cast<long long>(b) * C + i) * D, D, x.n_tab, c.err)) return;
+  uint4 lo = ld16(x.k, src + kc * 8, x.n_kv, c.err);
+  uint4 hi = ld16(x.k, src + D / 2 + kc * 8, x.n_kv, c.err);
   const float* cr = x.cos + (static_cast<size_t>(b) * C + i) * D;
   const float* sr = x.sin + (static_cast<size_t>(b) * C + i) * D;
-  uint4 vl = ld16(x.v + src + kc * 8), vh = ld16(x.v + src + D / 2 + kc * 8);
+  uint4 vl = ld16(x.v, src + kc * 8, x.n_kv, c.err), vh = ld16(x.v, src + D / 2 + kc * 8, x.n_kv, c.err);
   if (c.f16) {
     rope_pair<true>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
     vl = bf16x8_to_f16x8(vl);
@@ -47,10 +54,10 @@ __device__ __forceinline__ void put_new_row(const CacheView& c, const ChunkView&
     rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
   }
   const size_t d = crow(c, b, h, dst);
-  st16(c.k + d + kc * 8, lo);
-  st16(c.k + d + D / 2 + kc * 8, hi);
-  st16(c.v + d + kc * 8, vl);
-  st16(c.v + d + D / 2 + kc * 8, vh);
+  st16(c.k, d + kc * 8, c.extent, lo, c.err);
+  st16(c.k, d + D / 2 + kc * 8, c.extent, hi, c.err);
+  st16(c.v, d + kc * 8, c.extent, vl, c.err);
+  st16(c.v, d + D / 2 + kc * 8, c.extent, vh, c.err);
 }
 
 __device__ __forceinline__ int clamp_rows(int n, int C, int32_t* err, bool report) {
@@ -133,8 +140,9 @@ __global__ void sliding_stage(CacheView c, const int32_t* n_rows, int B, int Hkv
     if (!ok || e == 0 || row >= cnt) continue;
     const size_t s = crow(c, b, h, S + e + row) + cc * 8;
     const size_t d = ((static_cast<size_t>(b) * Hkv + h) * W + row) * D + cc * 8;
-    st16(stage_k + d, ld16(c.k + s));
-    st16(stage_v + d, ld16(c.v + s));
+    const long long nst = static_cast<long long>(B) * Hkv * W * D;
+    st16(stage_k, d, nst, ld16(c.k, s, c.extent, c.err), c.err);
+    st16(stage_v, d, nst, ld16(c.v, s, c.extent, c.err), c.err);
   }
 }
 
@@ -164,10 +172,11 @@ __global__ void sliding_commit(CacheView c, ChunkView x, int B, int Hkv, int D, 
       if (e == 0 || rr >= cnt) continue;
       const size_t s = ((static_cast<size_t>(b) * Hkv + h) * W + rr) * D;
       const size_t d = crow(c, b, h, S + rr);
-      st16(c.k + d + kc * 8, ld16(stage_k + s + kc * 8));
-      st16(c.k + d + D / 2 + kc * 8, ld16(stage_k + s + D / 2 + kc * 8));
-      st16(c.v + d + kc * 8, ld16(stage_v + s + kc * 8));
-      st16(c.v + d + D / 2 + kc * 8, ld16(stage_v + s + D / 2 + kc * 8));
+      const long long nst = static_cast<long long>(B) * Hkv * W * D;
+      st16(c.k, d + kc * 8, c.extent, ld16(stage_k, s + kc * 8, nst, c.err), c.err);
+      st16(c.k, d + D / 2 + kc * 8, c.extent, ld16(stage_k, s + D / 2 + kc * 8, nst, c.err), c.err);
+      st16(c.v, d + kc * 8, c.extent, ld16(stage_v, s + kc * 8, nst, c.err), c.err);
+      st16(c.v, d + D / 2 + kc * 8, c.extent, ld16(stage_v, s + D / 2 + kc * 8, nst, c.err), c.err);
     } else {
       const int t = rr - W;
       if (t >= n) continue;
@@ -213,8 +222,9 @@ __global__ void snapshot_kernel(CacheView c, const int32_t* n_real, int B, int H
     if (!ok || row >= e_pad - e_ex) continue;
     const size_t s = crow(c, b, h, S + e_ex + row) + cc * 8;
     const size_t d = ((static_cast<size_t>(b) * Hkv + h) * C + row) * D + cc * 8;
-    st16(saved_k + d, ld16(c.k + s));
-    st16(saved_v + d, ld16(c.v + s));
+    const long long nsv = static_cast<long long>(B) * Hkv * C * D;
+    st16(saved_k, d, nsv, ld16(c.k, s, c.extent, c.err), c.err);
+    st16(saved_v, d, nsv, ld16(c.v, s, c.extent, c.err), c.err);
   }
 }
 
@@ -250,8 +260,9 @@ __global__ void rollback_stage(CacheView c, int B, int Hkv, int D, int C, const 
     if (!good || d == 0 || row >= keep - S) continue;
     const size_t s = crow(c, b, h, S + row) + cc * 8;
     const size_t o = ((static_cast<size_t>(b) * Hkv + h) * W + row) * D + cc * 8;
-    st16(stage_k + o, ld16(c.k + s));
-    st16(stage_v + o, ld16(c.v + s));
+    const long long nst = static_cast<long long>(B) * Hkv * W * D;
+    st16(stage_k, o, nst, ld16(c.k, s, c.extent, c.err), c.err);
+    st16(stage_v, o, nst, ld16(c.v, s, c.extent, c.err), c.err);
   }
 }
 
@@ -285,15 +296,17 @@ __global__ void rollback_commit(CacheView c, int B, int Hkv, int D, int C, Hdr* 
       if (rr >= keep - S) continue;
       const size_t s = ((static_cast<size_t>(b) * Hkv + h) * W + rr) * D + cc * 8;
       const size_t o = crow(c, b, h, S + d + rr) + cc * 8;
-      st16(c.k + o, ld16(stage_k + s));
-      st16(c.v + o, ld16(stage_v + s));
+      const long long nst = static_cast<long long>(B) * Hkv * W * D;
+      st16(c.k, o, c.extent, ld16(stage_k, s, nst, c.err), c.err);
+      st16(c.v, o, c.extent, ld16(stage_v, s, nst, c.err), c.err);
     } else {
       const int t = rr - W;
       if (t >= d) continue;
       const size_t s = ((static_cast<size_t>(b) * Hkv + h) * C + t) * D + cc * 8;
       const size_t o = crow(c, b, h, S + t) + cc * 8;
-      st16(c.k + o, ld16(saved_k + s));
-      st16(c.v + o, ld16(saved_v + s));
+      const long long nsv = static_cast<long long>(B) * Hkv * C * D;
+      st16(c.k, o, c.extent, ld16(saved_k, s, nsv, c.err), c.err);
+      st16(c.v, o, c.extent, ld16(saved_v, s, nsv, c.err), c.err);
     }
   }
 }

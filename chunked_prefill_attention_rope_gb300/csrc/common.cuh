@@ -20,6 +20,45 @@ __device__ __forceinline__ void set_err(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
+// ------------------------------------------------------------------ checked builds
+
+// Built with CPA_BOUNDS_CHECK, every global access at an index the kernels
+// compute (TMA copies are bounded by their tensor maps) first checks that
+// [i, i + len) lies inside its buffer of n elements; otherwise it sets
+// CPA_EBIT_BOUNDS and skips the access (a load then reads zero).  Without the
+// flag the check folds away.
+#ifdef CPA_BOUNDS_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(long long i, long long len, long long n, int32_t* err) {
+  if (!kChecked) return true;
+  if (i >= 0 && len >= 0 && i + len <= n) return true;
+  if (err) atomicOr(err, CPA_EBIT_BOUNDS);
+  return false;
+}
+
+// Element i of `base` (n elements), or T{} when out of range.
+template <typename T>
+__device__ __forceinline__ T ld_chk(const T* base, long long i, long long n, int32_t* err) {
+  return in_bounds(i, 1, n, err) ? base[i] : T{};
+}
+template <typename T>
+__device__ __forceinline__ void st_chk(T* base, long long i, long long n, T v, int32_t* err) {
+  if (in_bounds(i, 1, n, err)) base[i] = v;
+}
+// 16 bytes at elements [i, i + 16 / sizeof(E)) of `base` (n elements of E).
+template <typename E>
+__device__ __forceinline__ uint4 ld16_chk(const E* base, long long i, long long n, int32_t* err) {
+  return in_bounds(i, 16 / sizeof(E), n, err) ? *reinterpret_cast<const uint4*>(base + i) : make_uint4(0, 0, 0, 0);
+}
+template <typename E>
+__device__ __forceinline__ void st16_chk(E* base, long long i, long long n, uint4 v, int32_t* err) {
+  if (in_bounds(i, 16 / sizeof(E), n, err)) *reinterpret_cast<uint4*>(base + i) = v;
+}
+
 // Warp-uniform agreement: true only if every lane of the warp passes true.
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
@@ -103,8 +142,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Wall-clock bound of one pipeline wait.  Every legitimate wait in these
 // kernels ends within microseconds; this only turns a logic error into an
-// error flag instead of a hung GPU.
+// error flag instead of a hung GPU.  The checked build's test hooks make a
+// wait run out on purpose, so there the bound is shorter.
+#ifdef CPA_TEST_HOOKS
+constexpr uint64_t kWaitLimitNs = 20ull * 1000ull * 1000ull;
+constexpr bool kTestHooks = true;
+#else
 constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+constexpr bool kTestHooks = false;
+#endif
 
 // Wait for the phase with the given parity to complete.  Returns false (and
 // raises *abort) when the wait runs out or another thread already aborted.

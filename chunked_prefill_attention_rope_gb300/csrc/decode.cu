@@ -160,12 +160,15 @@ __global__ void __launch_bounds__(kDThreads, 2)
   // Q fragments, rotated (rows >= G are zero).
   uint32_t qa[KS][4];
   {
-    const float* cr = p.cos + static_cast<size_t>(b) * D;
-    const float* sr = p.sin + static_cast<size_t>(b) * D;
+    // checked builds: an out-of-range table row reads as zeros
+    const bool tab_ok = in_bounds(static_cast<long long>(b) * D, D, n_tab(p), p.err);
+    const float* cr = p.cos + (tab_ok ? static_cast<size_t>(b) * D : 0);
+    const float* sr = p.sin + (tab_ok ? static_cast<size_t>(b) * D : 0);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int g = r0 + 8 * half;
-      const bool ok = g < p.G;
+      const bool ok = g < p.G && tab_ok &&
+                      in_bounds((static_cast<long long>(b) * p.Hq + kvh * p.G + g) * D, D, n_qo(p), p.err);
       const uint16_t* qrow = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G + (ok ? g : 0)) * D;
 #pragma unroll
       for (int k = 0; k < KS / 2; ++k) {
@@ -203,8 +206,8 @@ __global__ void __launch_bounds__(kDThreads, 2)
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int g = r0 + 8 * half;
-      if (g < p.G)
-        mrow[half] = p.mask + (static_cast<size_t>(b) * p.Hq + kvh * p.G + g) * static_cast<size_t>(p.P + p.C);
+      const long long mo = (static_cast<long long>(b) * p.Hq + kvh * p.G + g) * (static_cast<long long>(p.P) + p.C);
+      if (g < p.G && in_bounds(mo, static_cast<long long>(p.P) + p.C, n_mask(p), p.err)) mrow[half] = p.mask + mo;
     }
   }
   const uint32_t kbase = smem_u32(smem + CF::kK);
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(kDThreads, 2)
         uint4* plo = reinterpret_cast<uint4*>(ktile + tile_off(r, kc));
         uint4* phi = reinterpret_cast<uint4*>(ktile + tile_off(r, kh));
         uint4 lo = *plo, hi = *phi;
+        if (!in_bounds((static_cast<long long>(b) * p.C + base + r) * D, D, n_tab(p), p.err)) continue;
         const float* cr = p.cos + (static_cast<size_t>(b) * p.C + base + r) * D;
         const float* sr = p.sin + (static_cast<size_t>(b) * p.C + base + r) * D;
         rope_pair<F16>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
@@ -402,7 +406,11 @@ __global__ void __launch_bounds__(kDThreads, 2)
       lsum = __fmaf_rn(wgt[w], ml[(w * 16 + row) * 2 + 1], lsum);
     }
     const float inv = empty ? 0.f : 1.f / lsum;
-    if (g < p.G) {
+    const bool rows_ok =
+        g < p.G && in_bounds(static_cast<long long>(b * p.Hq + kvh * p.G + g) * D, D, n_qo(p), p.err) &&
+        (!p.part_o || in_bounds((static_cast<long long>(split) * p.B * p.Hq + b * p.Hq + kvh * p.G + g) * D, D,
+                                p.n_part, p.err));
+    if (rows_ok) {
       const int h = kvh * p.G + g;
       const size_t orow = static_cast<size_t>(b) * p.Hq + h;  // C == 1
       const int sel = p.sel_row ? p.sel_row[b] : tp.n - 1;

@@ -114,7 +114,32 @@ struct AttnParams {
   uint8_t* tcls;     // [blocks * ntiles] tile classes (kTileDead / kTileBinary / kTileGeneral)
   int4* hull;        // [blocks] visited tiles: chunk [x, y), past [z, w) in the tile index space
   uint4* mbits;      // [B, Hq, ntiles, C] visibility bits of each row and tile, or null
+  // Checked builds: element counts of the buffers whose size the shapes alone
+  // do not give, and the test hook.
+  long long n_part;     // part_o elements (part_lse holds n_part / D)
+  long long n_app;      // fused append: elements the cache's K (and V) view spans
+  int test_drop_tile;   // K/V tile whose copy each CTA withholds (-1: none)
 };
+
+// Element counts of an attention call's buffers (checked builds).
+__host__ __device__ inline long long n_qo(const AttnParams& p) {  // q, out, rotated q
+  return static_cast<long long>(p.B) * p.Hq * p.C * p.D;
+}
+__host__ __device__ inline long long n_chunk(const AttnParams& p) {  // k_new, v_new, rotated k, half v
+  return static_cast<long long>(p.B) * p.Hkv * p.C * p.D;
+}
+__host__ __device__ inline long long n_tab(const AttnParams& p) {  // cos, sin
+  return static_cast<long long>(p.B) * p.C * p.D;
+}
+__host__ __device__ inline long long n_mask(const AttnParams& p) {
+  return static_cast<long long>(p.B) * p.Hq * p.C * (static_cast<long long>(p.P) + p.C);
+}
+__host__ __device__ inline long long n_sel(const AttnParams& p) {  // out_sel
+  return static_cast<long long>(p.B) * p.Hq * p.D;
+}
+__host__ __device__ inline long long n_bits(const AttnParams& p) {  // mbits (uint4)
+  return static_cast<long long>(p.B) * p.Hq * p.ntiles * p.C;
+}
 
 
 // Team-aligned stream-K layout for these sizes, and its workspace.
@@ -157,7 +182,9 @@ struct CacheView {
   int64_t sb, sh, ss;  // strides in elements
   int32_t* len;
   int cap, window, sink;
-  int f16;  // elements are IEEE half (else bf16)
+  int f16;             // elements are IEEE half (else bf16)
+  long long extent;    // elements the K (and V) view spans (checked builds)
+  int32_t* err;        // the call's error word (checked builds)
 };
 
 struct ChunkView {
@@ -166,6 +193,7 @@ struct ChunkView {
   const float* cos;   // [B, C, D]
   const float* sin;
   const int32_t* n_rows;
+  long long n_kv, n_tab;  // elements of k (and v) and of cos (and sin) (checked builds)
 };
 
 // Scratch layout of a sliding cache (byte offsets from the scratch base).

@@ -143,6 +143,9 @@ __device__ __forceinline__ void fused_append_pair(const AttnParams& p, int b, in
   const size_t dst = static_cast<size_t>(b) * p.app_sb + static_cast<size_t>(h) * p.app_sh +
                      static_cast<size_t>(L + i) * p.app_ss;
   const size_t src = ((static_cast<size_t>(b) * p.Hkv + h) * p.C + i) * D;
+  if (!in_bounds(static_cast<long long>(dst), D, p.n_app, p.err) ||
+      !in_bounds(static_cast<long long>(src), D, n_chunk(p), p.err))
+    return;
   *reinterpret_cast<uint4*>(p.app_k + dst + kc * 8) = lo;
   *reinterpret_cast<uint4*>(p.app_k + dst + D / 2 + kc * 8) = hi;
   uint4 vl = *reinterpret_cast<const uint4*>(p.v_new + src + kc * 8);

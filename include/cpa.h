@@ -58,6 +58,8 @@ typedef enum {
 #define CPA_EBIT_SLIDING_N 8      /* sliding append: n > W - S or len > W; sequence untouched */
 #define CPA_EBIT_SNAPSHOT 16      /* rollback: cache length does not match the snapshot */
 #define CPA_EBIT_TIMEOUT 32       /* a bounded in-kernel pipeline wait ran out */
+#define CPA_EBIT_BOUNDS 64        /* checked builds only: a computed index fell outside
+                                     its buffer; the access was skipped */
 
 enum { CPA_CACHE_GLOBAL = 0, CPA_CACHE_SLIDING = 1 };
 /* Element format of a cache's K and V ([P4, Declined with rationale] names a

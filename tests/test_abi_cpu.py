@@ -31,6 +31,20 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(so, name), name
 
 
+def test_checked_build_exports_the_same_symbols_and_its_hook(lib):
+    """libcpa_checked.so (bounds checks and test hooks) exports every cpa.h
+    entry point and cpa_test_drop_tile (include/cpa_test.h); the library
+    itself has no test hook."""
+    cpa, so = lib
+    checked = cpa.load_library("checked")
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    assert hasattr(checked, "cpa_test_drop_tile")
+    assert not hasattr(so, "cpa_test_drop_tile")
+    hdr = open(os.path.join(ROOT, "include", "cpa_test.h")).read()
+    assert re.findall(r"\b(cpa_[a-z_]+)\s*\(", re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)) == ["cpa_test_drop_tile"]
+
+
 def test_status_strings_and_version(lib):
     _, so = lib
     assert so.cpa_status_str(0) == b"ok"
@@ -108,10 +122,12 @@ def test_sliding_guards(lib):
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import chunked_prefill_attention_rope_gb300 as cpa
-    monkeypatch.setattr(cpa, "_LIB", None)
-    monkeypatch.setattr(cpa, "lib_path", lambda: str(tmp_path / "missing.so"))
+    monkeypatch.setattr(cpa, "_LIBS", {})
+    monkeypatch.setattr(cpa, "lib_path", lambda variant=None: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         cpa.load_library()
+    with pytest.raises(RuntimeError):
+        cpa.load_library("checked")
 
 
 def test_tail_plan_policy(lib):

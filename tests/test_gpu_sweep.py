@@ -9,8 +9,8 @@ single-tile with and without a cluster merge, one-token decode).  Each case
 runs the implicit mask and the explicit mask built from the same rule
 ("functiongemma: chunk prefill-with-past graph", Change: per-head additive mask
 over past + C keys) and checks both against the oracle (max-abs 1e-2, rel-L2
-3e-3), the selected-row argmax, and the two masks against each other (bitwise,
-or within the output tolerance on the two-tile kernel).
+3e-3), the selected-row argmax, and the two masks against each other
+(bitwise).
 """
 import numpy as np
 import pytest
