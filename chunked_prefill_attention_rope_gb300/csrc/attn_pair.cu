@@ -48,11 +48,16 @@ namespace {
 constexpr int kBN = 128;
 constexpr int kThreadsPair = 384;
 // Register split (setmaxnreg): the launch gives every thread 168 registers
-// (384 x 168 = 64512).  The aux warpgroup (warps 8-11) drops to 96, freeing
-// 128 x 72 = 9216; the two softmax warpgroups rise to 200, taking
-// 2 x 128 x 32 = 8192 <= 9216, so the increase never waits on the pool.
+// (384 x 168 = 64512).  The aux warpgroup (warps 8-11) drops to 96 (104 at
+// D = 128, whose producer and MMA issuer keep more state), freeing 128 x 72
+// = 9216 (128 x 64 = 8192); the two softmax warpgroups rise to 200, taking
+// 2 x 128 x 32 = 8192, so the increase never waits on the pool.
 constexpr int kRegsSoftmax = 200;
-constexpr int kRegsAux = 96;
+template <int D>
+struct RegsAux {
+  static constexpr int value = D == 128 ? 104 : 96;
+};
+static_assert(2 * 128 * (kRegsSoftmax - 168) <= 128 * (168 - RegsAux<128>::value), "register split");
 constexpr int kUnitRows = 256;
 // A unit switch (Q reload, epilogue, pipeline refill) costs about this many key
 // tiles (per-CTA cycle counts fitted over key tiles and segments: ~3); the
@@ -83,6 +88,7 @@ struct PairCfg {
 
 struct __align__(8) PairBars {
   uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t v_ready[4];  // implicit mask: V tile landed and its dead rows cleared (warp 11)
   uint64_t s_full[2], p_full[2], o_done[2], q_full[2], q_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -595,6 +601,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_ready[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   walk.init(p, cta);
 
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsAux));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegsAux<D>::value));
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -728,7 +735,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int jj = 0; jj < n; ++jj) {
           const int gt = g + jj;
           const int st = gt % NS;
-          if (!(ok = mbar_wait(&bars->p_full[0], gt & 1, abort) && mbar_wait(&bars->v_full[st], (gt / NS) & 1, abort)))
+          if (!(ok = mbar_wait(&bars->p_full[0], gt & 1, abort) &&
+                     mbar_wait(EXPLICIT ? &bars->v_full[st] : &bars->v_ready[st], (gt / NS) & 1, abort)))
             break;
           tc_fence_after();
           issue_pv(0, gt, jj == 0);
@@ -782,7 +790,35 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         while (!mbar_try_wait(&bars->q_full[qi], (seg - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
     }
-  }  // warp 11: no role
+  } else if (!EXPLICIT) {
+    // ------------------------------------------------------------ V tile release (warp 11)
+    // Implicit mask: once a V tile has landed, its dead rows (cache slots
+    // past the length, chunk pad rows) are cleared, since P is exactly zero
+    // there but 0 times a non-finite value is not; then the tile goes to the
+    // P V products.  (With an explicit mask every visited row must hold
+    // finite values and the products take the tile as it lands.)
+    int g = 0;
+    bool ok = true;
+    int unit, a, e;
+    Block bx;
+    while (ok && walk.next(unit, bx, a, e)) {
+      const TilePlan tp = block_plan(p, bx);
+      for (int j = a; j < e; ++j, ++g) {
+        const int st = g % NS;
+        if (!(ok = warp_all(mbar_wait(&bars->v_full[st], (g / NS) & 1, abort)))) break;
+        const int t = tp.index(j);
+        const bool chunk = t < tp.Tc;
+        int z0, z1;
+        dead_rows<kBN>(p, tp, chunk, (chunk ? t : t - tp.Tc) * kBN, z0, z1);
+        if (z0 < z1) {
+          zero_tile_rows<D>(sV + st * CF::kVBytes, kBN, z0, z1, lane, 32);
+          fence_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->v_ready[st]);
+      }
+    }
+  }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax (query tile qi)
@@ -947,19 +983,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             pv[q + 1] = fast_exp2(y.y);
           }
           emit(pv, c);
-        }
-        if (!EXPLICIT && qi == 0) {
-          // this tile's dead V rows (cache slots past the length, chunk pad
-          // rows) are cleared once the tile has landed and before either P V
-          // product reads it (both wait for this warpgroup's P)
-          int z0, z1;
-          dead_rows<kBN>(p, tp, chunk, base, z0, z1);
-          if (z0 < z1) {
-            const int st = gt % NS;
-            if (!(ok = warp_all(mbar_wait(&bars->v_full[st], (gt / NS) & 1, abort)))) break;
-            zero_tile_rows<D>(sV + st * CF::kVBytes, kBN, z0, z1, row, 128);
-            fence_async_smem();
-          }
         }
         const float sum = __fadd_rn(__fadd_rn(accA.x, accA.y), __fadd_rn(accB.x, accB.y));
         tmem_st_wait();

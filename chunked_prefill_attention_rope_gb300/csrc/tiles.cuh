@@ -125,6 +125,7 @@ template <int D>
 __device__ __forceinline__ void zero_tile_rows(uint8_t* tile, int rows, int r0, int r1, int tid, int nthreads) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   const int n = (r1 - r0) * kChunks;
+#pragma unroll 1
   for (int k = tid; k < n; k += nthreads) {
     const int r = r0 + k / kChunks, c = k % kChunks;
     *reinterpret_cast<uint4*>(tile + (c / 8) * (rows * 128) + r * 128 + (c % 8) * 16) = make_uint4(0, 0, 0, 0);
