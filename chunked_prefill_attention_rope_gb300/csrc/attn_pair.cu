@@ -396,18 +396,21 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParam
   const int k0 = 4 * lane;
   bool live = false, general = false;
   for (int r0 = warp * 32; r0 < rows; r0 += kScanThreads) {
+    // lane l owns row r0 + l: its head and chunk row, and its offset in the
+    // mask (one division per 32 rows; each row's offset reaches the warp by
+    // shuffle)
+    const int rl = r0 + lane;
+    const int hl = x.kvh * p.G + rl / ni, il = i0 + rl % ni;
+    const long long ro_l = (static_cast<long long>(x.b * p.Hq + hl) * p.C + il) * stride + moff;
     uint4 mine = make_uint4(0u, 0u, 0u, 0u);  // bits of row r0 + lane
     for (int j0 = 0; j0 < 32 && r0 + j0 < rows; j0 += kScanBatch) {
       float v[kScanBatch][4];
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u) {
-        const int r = r0 + j0 + u;
+        const long long ro = __shfl_sync(0xffffffffu, ro_l, j0 + u);
         v[u][0] = v[u][1] = v[u][2] = v[u][3] = -1e30f;
-        if (r < rows) {
-          const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
-          const long long ro = (static_cast<long long>(x.b * p.Hq + h) * p.C + i) * stride + moff;
+        if (r0 + j0 + u < rows && in_bounds(ro, lim, n_mask(p), p.err)) {
           const float* row = p.mask + ro;
-          if (!in_bounds(ro, lim, n_mask(p), p.err)) continue;
           if (vec) {
             if (k0 < lim) {
               const float4 f = __ldg(reinterpret_cast<const float4*>(row + k0));
@@ -436,11 +439,8 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParam
         if (lane == j0 + u) mine = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    if (p.mbits && r0 + lane < rows) {
-      const int r = r0 + lane;
-      const int h = x.kvh * p.G + r / ni, i = i0 + r % ni;
-      st_chk(p.mbits, (static_cast<long long>(x.b * p.Hq + h) * T + t) * p.C + i, n_bits(p), mine, p.err);
-    }
+    if (p.mbits && rl < rows)
+      st_chk(p.mbits, (static_cast<long long>(x.b * p.Hq + hl) * T + t) * p.C + il, n_bits(p), mine, p.err);
   }
   live = __syncthreads_or(live);
   general = __syncthreads_or(general);
