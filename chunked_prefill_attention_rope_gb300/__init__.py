@@ -139,9 +139,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device: torch.device) -> Optional[int]:
+    """The cudaStream_t of `stream`, or of torch's current stream on `device`."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        if _raw_stream is not None:
+            return _raw_stream(device.index if device.index is not None else torch.cuda.current_device())
+        return torch.cuda.current_stream(device).cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -151,9 +157,9 @@ def new_error_word(device="cuda") -> torch.Tensor:
 
 
 def _need(t: torch.Tensor, name: str, dtype, shape=None):
-    if t.dtype != dtype:
+    if t.dtype is not dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
@@ -173,11 +179,13 @@ class KVCache:
         self.k, self.v, self.len = k, v, length
         self.kind, self.window, self.sink = kind, window, sink
         self.B, self.Hkv, self.cap, self.D = k.shape
+        # the C struct is built once: a KVCache describes fixed tensors
+        self._struct = _Cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), k.stride(2), length.data_ptr(),
+                              self.cap, kind, window, sink, 1 if k.dtype == torch.float16 else 0)
+        self._ref = ctypes.byref(self._struct)
 
     def struct(self) -> _Cache:
-        return _Cache(self.k.data_ptr(), self.v.data_ptr(), self.k.stride(0), self.k.stride(1),
-                      self.k.stride(2), self.len.data_ptr(), self.cap, self.kind, self.window, self.sink,
-                      1 if self.k.dtype == torch.float16 else 0)
+        return self._struct
 
 
 def attn_workspace_size(B, Hq, Hkv, D, C, P) -> int:
@@ -190,8 +198,7 @@ def attn_workspace_size_mask(B, Hq, Hkv, D, C, P) -> int:
 
 
 def cache_scratch_size(cache: KVCache, C: int) -> int:
-    s = cache.struct()
-    return int(load_library().cpa_cache_scratch_size(ctypes.byref(s), cache.B, cache.Hkv, cache.D, C))
+    return int(load_library().cpa_cache_scratch_size(cache._ref, cache.B, cache.Hkv, cache.D, C))
 
 
 def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
@@ -201,37 +208,48 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
     lib = load_library()
     B, Hq, C, D = q.shape
     Hkv = k_new.shape[1]
-    _need(q, "q", torch.bfloat16)
-    _need(k_new, "k_new", torch.bfloat16, (B, Hkv, C, D))
-    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, C, D))
-    _need(cos, "cos", torch.float32, (B, C, D))
-    _need(sin, "sin", torch.float32, (B, C, D))
+    dev = q.device
+    bf16, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    kv_shape, tab_shape, row_shape = (B, Hkv, C, D), (B, C, D), (B,)
+    _need(q, "q", bf16)
+    _need(k_new, "k_new", bf16, kv_shape)
+    _need(v_new, "v_new", bf16, kv_shape)
+    _need(cos, "cos", f32, tab_shape)
+    _need(sin, "sin", f32, tab_shape)
     if mask is not None:
-        _need(mask, "mask", torch.float32, (B, Hq, C, P + C))
-    for t, name in ((past_len, "past_len"), (n_real, "n_real"), (sel_row, "sel_row")):
-        if t is not None:
-            _need(t, name, torch.int32, (B,))
+        _need(mask, "mask", f32, (B, Hq, C, P + C))
+    if past_len is not None:
+        _need(past_len, "past_len", i32, row_shape)
+    if n_real is not None:
+        _need(n_real, "n_real", i32, row_shape)
+    if sel_row is not None:
+        _need(sel_row, "sel_row", i32, row_shape)
     if out is None:
-        out = torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=q.device)
-    _need(out, "out", torch.bfloat16, (B, Hq, C, D))
-    if out_sel is None and want_sel:
-        out_sel = torch.empty((B, Hq * D), dtype=torch.float32, device=q.device)
-    need = (lib.cpa_attn_workspace_size_mask if mask is not None else lib.cpa_attn_workspace_size)(B, Hq, Hkv, D, C, P)
-    if workspace is None and need > 0 and alloc_workspace:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    if err is None:
-        err = new_error_word(q.device)
-    cs = cache.struct()
-    a = _AttnArgs(B, Hq, Hkv, D, C, P, float(scale), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                  cos.data_ptr(), sin.data_ptr(), ctypes.pointer(cs), _ptr(mask), _ptr(past_len),
-                  _ptr(n_real), int(window), 1 if causal else 0, _ptr(sel_row), out.data_ptr(),
-                  _ptr(out_sel), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                  err.data_ptr(), int(sm_budget))
-    if append_rows is not None:
-        _need(append_rows, "n_rows", torch.int32, (B,))
-        _check(getattr(lib, entry)(ctypes.byref(a), append_rows.data_ptr(), _stream(stream)))
+        out = torch.empty((B, Hq, C, D), dtype=bf16, device=dev)
     else:
-        _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream)))
+        _need(out, "out", bf16, q.shape)
+    if out_sel is None and want_sel:
+        out_sel = torch.empty((B, Hq * D), dtype=f32, device=dev)
+    if workspace is None and alloc_workspace:
+        size = lib.cpa_attn_workspace_size_mask if mask is not None else lib.cpa_attn_workspace_size
+        need = size(B, Hq, Hkv, D, C, P)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = new_error_word(dev)
+    a = _AttnArgs(B, Hq, Hkv, D, C, P, float(scale), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                  cos.data_ptr(), sin.data_ptr(), ctypes.pointer(cache._struct),
+                  None if mask is None else mask.data_ptr(), None if past_len is None else past_len.data_ptr(),
+                  None if n_real is None else n_real.data_ptr(), int(window), 1 if causal else 0,
+                  None if sel_row is None else sel_row.data_ptr(), out.data_ptr(),
+                  None if out_sel is None else out_sel.data_ptr(),
+                  None if workspace is None else workspace.data_ptr(),
+                  0 if workspace is None else workspace.numel(), err.data_ptr(), int(sm_budget))
+    if append_rows is not None:
+        _need(append_rows, "n_rows", i32, row_shape)
+        _check(getattr(lib, entry)(ctypes.byref(a), append_rows.data_ptr(), _stream(stream, dev)))
+    else:
+        _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream, dev)))
     return out, out_sel
 
 
@@ -268,19 +286,21 @@ def kv_append(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch=None, err=
     """Append rows [0, n_rows[b]) of the chunk (K rotated, V copied) to the cache."""
     lib = load_library()
     B, Hkv, C, D = k_new.shape
+    kv_shape, tab_shape = (B, Hkv, C, D), (B, C, D)
     _need(k_new, "k_new", torch.bfloat16)
-    _need(v_new, "v_new", torch.bfloat16, (B, Hkv, C, D))
-    _need(cos, "cos", torch.float32, (B, C, D))
-    _need(sin, "sin", torch.float32, (B, C, D))
+    _need(v_new, "v_new", torch.bfloat16, kv_shape)
+    _need(cos, "cos", torch.float32, tab_shape)
+    _need(sin, "sin", torch.float32, tab_shape)
     _need(n_rows, "n_rows", torch.int32, (B,))
+    dev = k_new.device
     if err is None:
-        err = new_error_word(k_new.device)
-    cs = cache.struct()
+        err = new_error_word(dev)
     if scratch is None and cache.kind == SLIDING:
-        scratch = torch.empty(cache_scratch_size(cache, C), dtype=torch.uint8, device=k_new.device)
-    _check(lib.cpa_kv_append(ctypes.byref(cs), k_new.data_ptr(), v_new.data_ptr(), cos.data_ptr(),
-                             sin.data_ptr(), n_rows.data_ptr(), B, Hkv, D, C, _ptr(scratch),
-                             0 if scratch is None else scratch.numel(), err.data_ptr(), _stream(stream)))
+        scratch = torch.empty(cache_scratch_size(cache, C), dtype=torch.uint8, device=dev)
+    _check(lib.cpa_kv_append(cache._ref, k_new.data_ptr(), v_new.data_ptr(), cos.data_ptr(),
+                             sin.data_ptr(), n_rows.data_ptr(), B, Hkv, D, C,
+                             None if scratch is None else scratch.data_ptr(),
+                             0 if scratch is None else scratch.numel(), err.data_ptr(), _stream(stream, dev)))
     return err
 
 
@@ -290,10 +310,9 @@ def kv_snapshot_padded_append(cache: KVCache, n_real, C: int, scratch, err=None,
     _need(n_real, "n_real", torch.int32, (cache.B,))
     if err is None:
         err = new_error_word(n_real.device)
-    cs = cache.struct()
-    _check(lib.cpa_kv_snapshot_padded_append(ctypes.byref(cs), n_real.data_ptr(), cache.B, cache.Hkv,
+    _check(lib.cpa_kv_snapshot_padded_append(cache._ref, n_real.data_ptr(), cache.B, cache.Hkv,
                                              cache.D, C, scratch.data_ptr(), scratch.numel(),
-                                             err.data_ptr(), _stream(stream)))
+                                             err.data_ptr(), _stream(stream, n_real.device)))
     return err
 
 
@@ -302,10 +321,9 @@ def kv_rollback_padded_append(cache: KVCache, C: int, scratch, err=None, stream=
     lib = load_library()
     if err is None:
         err = new_error_word(cache.len.device)
-    cs = cache.struct()
-    _check(lib.cpa_kv_rollback_padded_append(ctypes.byref(cs), cache.B, cache.Hkv, cache.D, C,
+    _check(lib.cpa_kv_rollback_padded_append(cache._ref, cache.B, cache.Hkv, cache.D, C,
                                              scratch.data_ptr(), scratch.numel(), err.data_ptr(),
-                                             _stream(stream)))
+                                             _stream(stream, cache.len.device)))
     return err
 
 
