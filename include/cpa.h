@@ -75,7 +75,9 @@ enum { CPA_KV_BF16 = 0, CPA_KV_F16 = 1 };
  *           rows, then the newest rows in chronological order; an append that
  *           overflows evicts the oldest non-sink rows and compacts.
  * Rows at or beyond len[b] are dead: the library never promises their bytes
- * ([P4, Declined with rationale]: nothing reads past the length).
+ * ([P4, Declined with rationale]: nothing reads past the length).  With the
+ * implicit mask their bytes never reach an output, whatever they hold (NaN
+ * and infinity patterns included); the same holds for the chunk's pad rows.
  * dtype CPA_KV_F16: K and V hold IEEE half values.  Appends round the fp32
  * rotation of each key (the same arithmetic as for bf16) to half, nearest
  * even, and convert value rows bf16 -> half (exact inside the half range;
@@ -127,9 +129,10 @@ typedef struct {
  *            ([P4, Fix]: pinned sink rows, chronological compaction).
  *          non-NULL: explicit additive fp32 mask [B, Hq, C, P + C],
  *            contiguous, 0 = attend, -1e30 = masked ([P1, Change]); entries
- *            <= -1e29 count as masked; entries are added to the scaled
- *            scores.  Every cache slot in [0, P) and every chunk row must then
- *            hold finite values.
+ *            <= -1e29 (or not a number) count as masked; other entries are
+ *            added to the scaled scores.  Every cache slot in [0, P) and every
+ *            chunk row must then hold finite values.  The explicit and the
+ *            implicit form of one mask give identical output bits.
  *   past_len, n_real  device int32 [B]; required for the implicit mask;
  *          n_real also gives the default selected row.  Out-of-range values
  *          are clamped and flagged (CPA_EBIT_PAST_GT_SPAN / _NREAL_GT_C).
@@ -143,7 +146,9 @@ typedef struct {
  *          bf16 rounding.
  *   workspace  device memory of at least cpa_attn_workspace_size(...) bytes
  *          (the work plan the call builds on the device, split-KV partial
- *          results, rotated copies of the chunk's queries and keys); may be
+ *          results, rotated copies of the chunk's queries and keys; with an
+ *          explicit mask, the classes of its key tiles and, given
+ *          cpa_attn_workspace_size_mask(...) bytes, its bit copy); may be
  *          NULL when that size is 0.  Its contents need no initialisation
  *          and are meaningless after the call.
  *   err    device int32 error word (required).
