@@ -213,6 +213,9 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
       (a->mask && !aligned16(a->mask)) || !aligned16(a->err))
     return CPA_ERR_ALIGN;
   if (static_cast<long long>(a->B) * a->Hq * a->C * a->D > (1LL << 40)) return CPA_ERR_SHAPE;
+  // the RoPE pre-passes index their items (rows x 16-byte chunk pairs, four
+  // heads per item) in 32 bits
+  if (static_cast<long long>(a->B) * (a->Hq + a->Hkv + 3) * a->C * (a->D / 16) >= (1LL << 31)) return CPA_ERR_SHAPE;
 
   const Geometry g = geometry(a->B, a->Hq, a->Hkv, a->D, a->C, a->P, a->sm_budget);
   const size_t need = workspace_bytes(g, a->B, a->Hq, a->Hkv, a->D, a->C, a->P);
@@ -348,6 +351,11 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   return CPA_OK;
 }
 
+// The cache kernels index their items (rows x 16-byte chunks) in 32 bits.
+bool items_fit(int B, int Hkv, long long rows, int D) {
+  return static_cast<long long>(B) * Hkv * rows * (D / 8) < (1LL << 31);
+}
+
 cpa_status chunk_check(const void* k_new, const void* v_new, const float* cos, const float* sin,
                        const int32_t* n_rows, int B, int Hkv, int D, int C, int32_t* err) {
   if (!k_new || !v_new || !cos || !sin || !n_rows || !err) return CPA_ERR_NULL;
@@ -410,6 +418,8 @@ cpa_status cpa_kv_append(const cpa_cache* cache, const void* k_new, const void* 
   cpa_status st = chunk_check(k_new, v_new, cos, sin, n_rows, B, Hkv, D, C, err);
   if (st != CPA_OK) return st;
   if ((st = check_cache(cache, D)) != CPA_OK) return st;
+  if (!items_fit(B, Hkv, static_cast<long long>(C) + (cache->kind == CPA_CACHE_SLIDING ? cache->window : 0), D))
+    return CPA_ERR_SHAPE;
   const CacheView cv = view_of(cache, B, Hkv, D, err);
   ChunkView x{static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), cos, sin, n_rows,
               static_cast<long long>(B) * Hkv * C * D, static_cast<long long>(B) * C * D};
@@ -437,6 +447,7 @@ cpa_status cpa_kv_snapshot_padded_append(const cpa_cache* cache, const int32_t* 
   if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
   const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
   if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
+  if (!items_fit(B, Hkv, static_cast<long long>(C) + cache->window, D)) return CPA_ERR_SHAPE;
   return launch_snapshot(view_of(cache, B, Hkv, D, err), n_real, B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CPA_OK
@@ -454,6 +465,7 @@ cpa_status cpa_kv_rollback_padded_append(const cpa_cache* cache, int B, int Hkv,
   if (cache->window <= C + cache->sink) return CPA_ERR_WINDOW_TOO_SMALL;
   const size_t need = sliding_scratch_layout(B, Hkv, D, C, cache->window).total;
   if (!scratch || scratch_bytes < need || !aligned16(scratch)) return CPA_ERR_WORKSPACE;
+  if (!items_fit(B, Hkv, static_cast<long long>(C) + cache->window, D)) return CPA_ERR_SHAPE;
   return launch_rollback(view_of(cache, B, Hkv, D, err), B, Hkv, D, C, static_cast<uint8_t*>(scratch), err,
                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CPA_OK

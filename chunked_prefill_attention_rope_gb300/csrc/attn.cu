@@ -668,12 +668,14 @@ __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
   grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
   const int D = p.D;
   const int HP = D / 16;
-  const long long total = static_cast<long long>(p.B) * p.Hkv * p.C * HP;
-  for (long long it = blockIdx.x * 256LL + threadIdx.x; it < total; it += static_cast<long long>(gridDim.x) * 256) {
-    const int kc = static_cast<int>(it % HP);
-    const long long r = it / HP;  // row of [B, Hkv, C]
-    const int i = static_cast<int>(r % p.C);
-    const int b = static_cast<int>(r / p.C / p.Hkv);
+  const int sh = __ffs(HP) - 1;  // HP is a power of two
+  const unsigned total = static_cast<unsigned>(p.B) * p.Hkv * p.C * HP;  // < 2^31 (host)
+  for (unsigned it = blockIdx.x * 256u + threadIdx.x; it < total; it += gridDim.x * 256u) {
+    const int kc = static_cast<int>(it & (HP - 1));
+    const unsigned rr = it >> sh;  // row of [B, Hkv, C]
+    const long long r = rr;
+    const int i = static_cast<int>(rr % static_cast<unsigned>(p.C));
+    const int b = static_cast<int>(rr / static_cast<unsigned>(p.C) / static_cast<unsigned>(p.Hkv));
     if (!in_bounds(r * D, D, n_chunk(p), p.err) ||
         !in_bounds((static_cast<long long>(b) * p.C + i) * D, D, n_tab(p), p.err))
       continue;

@@ -356,7 +356,13 @@ __device__ void plan_units(const AttnParams& p) {
     p.tlo[t] = t == teams ? T
                           : (whole ? p.ustart[deal_start(t, NB, teams)]
                                    : static_cast<int32_t>(static_cast<long long>(T) * t / teams));
-  if (threadIdx.x == 0) p.tlo[teams + 1] = whole ? 1 : 0;  // whole blocks: no unit is cut
+  int empty = 0;  // blocks without a live key tile (their units are zero-filled by the merge)
+  for (int u = threadIdx.x; u < NB; u += kPrepThreads) empty += cost[u] == 0;
+  empty = __syncthreads_count(empty > 0);
+  if (threadIdx.x == 0) {
+    p.tlo[teams + 1] = whole ? 1 : 0;  // whole blocks: no unit is cut
+    p.tlo[teams + 2] = empty;          // threads that saw an empty block
+  }
 }
 
 // Classes of a key tile of one block under an explicit mask.
@@ -485,18 +491,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
     return;
   }
   const int D = p.D;
-  const int HP = D / 16;  // 8-element chunk pairs (d, d + D/2) per row
+  const int HP = D / 16;  // 8-element chunk pairs (d, d + D/2) per row: 4, 8 or 16
+  const int hp_shift = D == 64 ? 2 : (D == 128 ? 3 : 4);
   const int HH = p.Hq + p.Hkv;
   const int groups = (HH + kPrepHeads - 1) / kPrepHeads;
-  const long long total = static_cast<long long>(p.B) * groups * p.C * HP;
-  const long long stride = static_cast<long long>(gridDim.x - 1) * blockDim.x;
-  for (long long it = (blockIdx.x - 1) * static_cast<long long>(blockDim.x) + threadIdx.x; it < total; it += stride) {
-    const int kc = static_cast<int>(it % HP);
-    long long t = it / HP;
-    const int i = static_cast<int>(t % p.C);
-    t /= p.C;
-    const int grp = static_cast<int>(t % groups);
-    const int b = static_cast<int>(t / groups);
+  // item index in 32 bits (the host keeps B * groups * C * HP below 2^31):
+  // a 64-bit division per item had made this pass issue-bound
+  const unsigned total = static_cast<unsigned>(p.B) * groups * p.C * HP;
+  const unsigned stride = (gridDim.x - 1) * blockDim.x;
+  for (unsigned it = (blockIdx.x - 1) * blockDim.x + threadIdx.x; it < total; it += stride) {
+    const int kc = static_cast<int>(it & (HP - 1));
+    unsigned t = it >> hp_shift;
+    const unsigned Cu = static_cast<unsigned>(p.C);
+    const int i = static_cast<int>(t % Cu);
+    t /= Cu;
+    const int grp = static_cast<int>(t % static_cast<unsigned>(groups));
+    const int b = static_cast<int>(t / static_cast<unsigned>(groups));
     const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
     const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
     if (!in_bounds((static_cast<long long>(b) * p.C + i) * D, D, n_tab(p), p.err)) continue;
@@ -1105,6 +1115,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_units_kernel(const Att
   grid_dependency_wait();  // partials and tags of attn_pair_kernel
   if (p.app_n && blockIdx.x == 0 && blockIdx.y == 0)  // fused append: every reader of len is done
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) fused_append_len(p, b);
+  // whole blocks dealt and none empty: no unit was cut, every row is written
+  if (PERM && p.tlo[p.teams + 1] && p.tlo[p.teams + 2] == 0) return;
   if (warp == 0) {
     const int gnat = (x.b * p.Hkv + x.kvh) * p.nblk + x.pair / p.team;
     int gblk = PERM ? p.upos[gnat] : gnat;  // the block's place in the walk order
@@ -1255,7 +1267,7 @@ PairWorkspace pair_workspace(int B, int Hq, int Hkv, int D, int C, int P, const 
   w.ustart = off; off += al((static_cast<size_t>(t.blocks) + 1) * sizeof(int32_t));
   w.uorder = off; off += al(static_cast<size_t>(t.blocks) * sizeof(int32_t));
   w.upos = off; off += al(static_cast<size_t>(t.blocks) * sizeof(int32_t));
-  w.tlo = off; off += al((static_cast<size_t>(t.teams) + 2) * sizeof(int32_t));  // + the whole-deal flag
+  w.tlo = off; off += al((static_cast<size_t>(t.teams) + 3) * sizeof(int32_t));  // + the whole-deal and empty flags
   w.part_o = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * D * sizeof(float));
   w.part_lse = off; off += al(static_cast<size_t>(ctas) * 2 * kUnitRows * sizeof(float));
   w.ptag = off; off += al(static_cast<size_t>(ctas) * 2 * sizeof(int32_t));

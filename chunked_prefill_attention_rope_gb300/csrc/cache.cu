@@ -74,11 +74,11 @@ __global__ void global_append_rows(CacheView c, ChunkView x, int B, int Hkv, int
   grid_launch_dependents();  // the next launch may be scheduled; it waits for this grid
   grid_dependency_wait();    // everything the launches before this one wrote
   const int HP = D / 16;
-  const long long total = static_cast<long long>(B) * Hkv * C * HP;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int kc = static_cast<int>(it % HP);
-    long long r = it / HP;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * C * HP;  // < 2^31 (host)
+  const int sh = __ffs(HP) - 1;  // HP is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int kc = static_cast<int>(it & (HP - 1));
+    unsigned r = it >> sh;
     const int i = static_cast<int>(r % C);
     r /= C;
     const int h = static_cast<int>(r % Hkv);
@@ -115,11 +115,11 @@ __global__ void sliding_stage(CacheView c, const int32_t* n_rows, int B, int Hkv
   grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
-  const long long total = static_cast<long long>(B) * Hkv * W * CH;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int cc = static_cast<int>(it % CH);
-    long long r = it / CH;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * W * CH;  // < 2^31 (host)
+  const int sh = __ffs(CH) - 1;  // CH is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int cc = static_cast<int>(it & (CH - 1));
+    unsigned r = it >> sh;
     const int row = static_cast<int>(r % W);
     r /= W;
     const int h = static_cast<int>(r % Hkv);
@@ -155,11 +155,11 @@ __global__ void sliding_commit(CacheView c, ChunkView x, int B, int Hkv, int D, 
   const int W = c.window, S = c.sink;
   const int HP = D / 16;
   const int rows = W + C;
-  const long long total = static_cast<long long>(B) * Hkv * rows * HP;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int kc = static_cast<int>(it % HP);
-    long long r = it / HP;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * rows * HP;  // < 2^31 (host)
+  const int sh = __ffs(HP) - 1;  // HP is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int kc = static_cast<int>(it & (HP - 1));
+    unsigned r = it >> sh;
     const int rr = static_cast<int>(r % rows);
     r /= rows;
     const int h = static_cast<int>(r % Hkv);
@@ -195,11 +195,11 @@ __global__ void snapshot_kernel(CacheView c, const int32_t* n_real, int B, int H
   grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
-  const long long total = static_cast<long long>(B) * Hkv * C * CH;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int cc = static_cast<int>(it % CH);
-    long long r = it / CH;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * C * CH;  // < 2^31 (host)
+  const int sh = __ffs(CH) - 1;  // CH is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int cc = static_cast<int>(it & (CH - 1));
+    unsigned r = it >> sh;
     const int row = static_cast<int>(r % C);
     r /= C;
     const int h = static_cast<int>(r % Hkv);
@@ -236,11 +236,11 @@ __global__ void rollback_stage(CacheView c, int B, int Hkv, int D, int C, const 
   grid_dependency_wait();    // everything the launches before this one wrote
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
-  const long long total = static_cast<long long>(B) * Hkv * W * CH;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int cc = static_cast<int>(it % CH);
-    long long r = it / CH;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * W * CH;  // < 2^31 (host)
+  const int sh = __ffs(CH) - 1;  // CH is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int cc = static_cast<int>(it & (CH - 1));
+    unsigned r = it >> sh;
     const int row = static_cast<int>(r % W);
     r /= W;
     const int h = static_cast<int>(r % Hkv);
@@ -276,11 +276,11 @@ __global__ void rollback_commit(CacheView c, int B, int Hkv, int D, int C, Hdr* 
   const int W = c.window, S = c.sink;
   const int CH = D / 8;
   const int rows = W + C;
-  const long long total = static_cast<long long>(B) * Hkv * rows * CH;
-  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < total;
-       it += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int cc = static_cast<int>(it % CH);
-    long long r = it / CH;
+  const unsigned total = static_cast<unsigned>(B) * Hkv * rows * CH;  // < 2^31 (host)
+  const int sh = __ffs(CH) - 1;  // CH is a power of two
+  for (unsigned it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    const int cc = static_cast<int>(it & (CH - 1));
+    unsigned r = it >> sh;
     const int rr = static_cast<int>(r % rows);
     r /= rows;
     const int h = static_cast<int>(r % Hkv);

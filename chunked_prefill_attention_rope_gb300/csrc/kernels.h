@@ -77,8 +77,8 @@ struct AttnParams {
   int perm;         // blocks walked in the planned order uorder, team ranges in tlo
   int32_t* uorder;  // [blocks] block at each walk position (perm)
   int32_t* upos;    // [blocks] walk position of each block (perm)
-  int32_t* tlo;     // [teams + 2] first cost position of each team's range, the total,
-                    // then 1 when whole blocks were dealt (perm)
+  int32_t* tlo;     // [teams + 3] first cost position of each team's range, the total,
+                    // then 1 when whole blocks were dealt, then whether a block is empty (perm)
   int units;        // B * Hkv * pairs
   int pairs;        // query-tile pairs per (sequence, kv head)
   int team;         // CTAs per team = pairs per block
