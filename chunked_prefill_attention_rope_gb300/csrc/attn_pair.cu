@@ -382,7 +382,7 @@ constexpr int kScanBatch = 8;  // mask rows a warp has in flight
 // visibility bits: word j, bit l holds key 4 l + j of the tile, set when the
 // entry is exactly 0 (the attention tests bit (q % 4, q / 4) for key q).
 // Keys past the row's end (P or C) read as masked.
-__global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kScanThreads, 4) mask_scan_kernel(const AttnParams p) {
   grid_launch_dependents();
   grid_dependency_wait();  // the mask may come from the work before this call
   const int T = p.ntiles;
