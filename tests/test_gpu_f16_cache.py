@@ -7,8 +7,9 @@ convert values to half (bit-exact against the oracle, global and sliding,
 through a padded tail with snapshot and rollback); the attention runs its
 products in fp16 on every path (two-tile, single-tile with and without a
 cluster, decode, explicit mask, fused append) and matches the oracle within
-the attention tolerance; explicit and implicit masks give the same bits
-(within the output tolerance on the two-tile kernel).
+the attention tolerance; explicit and implicit masks give the same bits; the
+fused attention + append matches the oracle's fp16 reading and its half
+append directly.
 """
 import numpy as np
 import pytest
@@ -155,3 +156,20 @@ def test_f16_fused_append_equals_attention_then_append(w):
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.int16) if a.dtype != torch.int32 else a,
                            b.view(torch.int16) if b.dtype != torch.int32 else b)
+    # and the fused call against the oracle directly: its fp16 reading of the
+    # attention, then its global append in half (cache rows [0, len) and len exact)
+    out, gk, gv, glen = outs[1]
+    host = {k: v.cpu() for k, v in inp.items()}
+    ck, cv = (t.to(torch.float16) for t in make_cache(w))
+    ref, _ = oracle_attn(host["q"], host["k"], host["v"], host["cos"], host["sin"], ck, cv, w.P,
+                         host["past_len"], host["n_real"], w.window, w.causal)
+    assert_close(out, ref, w.name + "/f16 fused")
+    ok_, ov_ = bits16(ck).copy(), bits16(cv).copy()
+    ol = host["past_len"].numpy().astype(np.int64).copy()
+    assert O.kv_append_global(ok_, ov_, ol, bf16_bits(host["k"]), bf16_bits(host["v"]), host["cos"].numpy(),
+                              host["sin"].numpy(), host["n_real"].numpy(), kv="f16") == []
+    assert glen.cpu().numpy().tolist() == ol.tolist()
+    for b in range(w.B):
+        n = int(ol[b])
+        assert np.array_equal(bits16(gk)[b, :, :n], ok_[b, :, :n])
+        assert np.array_equal(bits16(gv)[b, :, :n], ov_[b, :, :n])
