@@ -777,7 +777,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       const uint32_t q_bytes = (D / 64) * 128 * p.R * p.G;
-      int seg = 0;
+      int seg = 0, issued[2] = {-1, -1};  // last segment whose copy of each tile was issued
       bool ok = true;
       int unit, a, e;
       Block bx;
@@ -792,12 +792,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           for (int blk = 0; blk < D / 64; ++blk)
             tma_load_4d(sQ + blk * (128 * 128), &map_q, &bars->q_full[qi], blk * 64, (x.pair * 2 + qi) * p.R,
                         x.kvh * p.G, x.b);
+          issued[qi] = seg;
         }
         ++seg;
       }
-      for (int qi = 0; qi < 2 && seg > 0; ++qi) {  // let copies in flight land
+      for (int qi = 0; qi < 2; ++qi) {  // let copies in flight land (also those of a stopped segment)
+        if (issued[qi] < 0) continue;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&bars->q_full[qi], (seg - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_try_wait(&bars->q_full[qi], issued[qi] & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
     }
   } else if (!EXPLICIT) {
