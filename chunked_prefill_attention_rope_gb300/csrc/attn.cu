@@ -222,49 +222,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the tiles and waits (descriptors stay warp-uniform);
+    // one elected lane issues the MMAs and the commits that track them.
+    {
+      const bool leader = elect_lane();
       constexpr uint32_t idesc_qk = idesc_16(kBM, BN, false, F16);
       constexpr uint32_t idesc_pv = idesc_16(kBM, D, true, F16);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t p_addr = smem_u32(sP);
-      bool ok = my_nt > 0 ? mbar_wait(&bars->q_ready, 0, abort) : true;
+      bool ok = my_nt > 0 ? warp_all(mbar_wait(&bars->q_ready, 0, abort)) : true;
       auto issue_pv = [&](int q) -> bool {
         const int st = q % kStages;
-        if (!mbar_wait(&bars->p_full, q & 1, abort)) return false;
-        if (!mbar_wait(&bars->v_full[st], (q / kStages) & 1, abort)) return false;
+        if (!warp_all(mbar_wait(&bars->p_full, q & 1, abort))) return false;
+        if (!warp_all(mbar_wait(&bars->v_full[st], (q / kStages) & 1, abort))) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + st * SM::kVBytes);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(p_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, BN * 128, 1024);
-          mma_bf16_ss(tmem + SM::kOCol, a, bd, idesc_pv, (q > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(p_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, BN * 128, 1024);
+            mma_bf16_ss(tmem + SM::kOCol, a, bd, idesc_pv, (q > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->pv_done);
+          mma_commit(&bars->kv_empty[st]);
         }
-        mma_commit(&bars->pv_done);
-        mma_commit(&bars->kv_empty[st]);
+        __syncwarp();
         return true;
       };
       for (int q = 0; ok && q < my_nt; ++q) {
         const int st = q % kStages;
         const int sb = q & 1;
-        ok = mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort);
+        ok = warp_all(mbar_wait(&bars->k_full[st], (q / kStages) & 1, abort));
         if (!ok) break;
-        ok = mbar_wait(&bars->s_empty[sb], ((q >> 1) + 1) & 1, abort);
+        ok = warp_all(mbar_wait(&bars->s_empty[sb], ((q >> 1) + 1) & 1, abort));
         if (!ok) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * SM::kKBytes);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(q_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_addr + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-          mma_bf16_ss(tmem + SM::kSCol + sb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(q_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k_addr + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+            mma_bf16_ss(tmem + SM::kSCol + sb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[sb]);
         }
-        mma_commit(&bars->s_full[sb]);
+        __syncwarp();
         if (q > 0) ok = issue_pv(q - 1);
       }
       if (ok && my_nt > 0) issue_pv(my_nt - 1);
       // Every MMA issued above has finished once this barrier flips.
-      mma_commit(&bars->mma_done);
+      if (leader) mma_commit(&bars->mma_done);
+      __syncwarp();
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(&bars->mma_done, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }

@@ -695,18 +695,21 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the tiles and waits, so that every descriptor and
+    // TMEM address is a warp-uniform value; one lane, elected once, issues the
+    // MMAs and their commits (a commit tracks the MMAs of the lane that
+    // issues it).  Issuing from a lane-0-only loop instead cost ~64 clocks per
+    // MMA, as much as an MMA's tensor work at N = 128.
+    {
+      const bool leader = elect_lane();
       constexpr uint32_t idesc_qk = idesc_16(128, kBN, false, F16);
       constexpr uint32_t idesc_pv = idesc_16(128, D, true, F16);
       const uint32_t q_addr = smem_u32(smem + CF::kQ);
       int g = 0, seg = 0;
       bool ok = true;
       auto k_ready = [&](const TilePlan&, int, int gg) -> bool {
-        return mbar_wait(&bars->k_full[gg % NS], (gg / NS) & 1, abort);
+        return warp_all(mbar_wait(&bars->k_full[gg % NS], (gg / NS) & 1, abort));
       };
-      // Descriptors are formed once; the MMAs of a group step through them by
-      // constant offsets (the start-address field is address / 16), so the
-      // issuing thread spends as few instructions as possible between MMAs.
       const uint64_t qd0 = sdesc_sw128(q_addr, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vd0 = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
@@ -714,60 +717,70 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         const uint64_t qd = qd0 + static_cast<uint64_t>(i * (CF::kQBytes >> 4));
         const uint64_t kd = kd0 + static_cast<uint64_t>((gg % NS) * (CF::kKBytes >> 4));
         const uint32_t d_tm = tmem + i * kBN;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = ((kk / 4) * (128 * 128) + (kk % 4) * 32) >> 4;
-          const uint32_t ko = ((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4;
-          mma_bf16_ss(d_tm, qd + qo, kd + ko, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qo = ((kk / 4) * (128 * 128) + (kk % 4) * 32) >> 4;
+            const uint32_t ko = ((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4;
+            mma_bf16_ss(d_tm, qd + qo, kd + ko, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[i]);
         }
-        mma_commit(&bars->s_full[i]);
+        __syncwarp();
       };
       auto issue_pv = [&](int i, int gg, bool first) {
         const uint64_t vd = vd0 + static_cast<uint64_t>((gg % NS) * (CF::kVBytes >> 4));
         const uint32_t d_tm = tmem + CF::kOCol + i * D;
         const uint32_t p_tm = tmem + i * kBN;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(d_tm, p_tm + kk * 8, vd + static_cast<uint32_t>((kk * 2048) >> 4), idesc_pv,
-                      (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_bf16_ts(d_tm, p_tm + kk * 8, vd + static_cast<uint32_t>((kk * 2048) >> 4), idesc_pv,
+                        (!first || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (leader) mma_commit(bar);
+        __syncwarp();
       };
       int unit, a, e;
       Block bx;
       while (ok && walk.next(unit, bx, a, e)) {
         const TilePlan tp = block_plan(p, bx);
         const int n = e - a;
-        if (!(ok = k_ready(tp, a, g) && mbar_wait(&bars->q_full[0], seg & 1, abort))) break;
+        if (!(ok = k_ready(tp, a, g) && warp_all(mbar_wait(&bars->q_full[0], seg & 1, abort)))) break;
         tc_fence_after();
         issue_qk(0, g);
-        if (!(ok = mbar_wait(&bars->q_full[1], seg & 1, abort))) break;
+        if (!(ok = warp_all(mbar_wait(&bars->q_full[1], seg & 1, abort)))) break;
         tc_fence_after();
         issue_qk(1, g);
         for (int jj = 0; jj < n; ++jj) {
           const int gt = g + jj;
           const int st = gt % NS;
-          if (!(ok = mbar_wait(&bars->p_full[0], gt & 1, abort) &&
-                     mbar_wait(EXPLICIT ? &bars->v_full[st] : &bars->v_ready[st], (gt / NS) & 1, abort)))
+          if (!(ok = warp_all(mbar_wait(&bars->p_full[0], gt & 1, abort) &&
+                              mbar_wait(EXPLICIT ? &bars->v_full[st] : &bars->v_ready[st], (gt / NS) & 1, abort))))
             break;
           tc_fence_after();
           issue_pv(0, gt, jj == 0);
           if (jj + 1 == n) {
-            mma_commit(&bars->o_done[0]);
+            commit(&bars->o_done[0]);
           } else {
             if (!(ok = k_ready(tp, a + jj + 1, gt + 1))) break;
             tc_fence_after();
             issue_qk(0, gt + 1);
           }
-          if (!(ok = mbar_wait(&bars->p_full[1], gt & 1, abort))) break;
+          if (!(ok = warp_all(mbar_wait(&bars->p_full[1], gt & 1, abort)))) break;
           tc_fence_after();
           issue_pv(1, gt, jj == 0);
-          mma_commit(&bars->kv_empty[st]);
-          if (jj + 1 == n) mma_commit(&bars->o_done[1]);
+          commit(&bars->kv_empty[st]);
+          if (jj + 1 == n) commit(&bars->o_done[1]);
           else issue_qk(1, gt + 1);
         }
         g += n;
         ++seg;
       }
-      mma_commit(&bars->mma_done);
+      commit(&bars->mma_done);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(&bars->mma_done, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }

@@ -62,6 +62,20 @@ __device__ __forceinline__ void st16_chk(E* base, long long i, long long n, uint
 // Warp-uniform agreement: true only if every lane of the warp passes true.
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// One lane of a fully active warp (elect.sync, always the same lane for the
+// same mask).  A tensor-core issuer guards its MMAs with this rather than a
+// lane-index test: the rest of the warp walks the same loop, so descriptors
+// stay warp-uniform values and each MMA issues with little overhead.
+__device__ __forceinline__ bool elect_lane() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
