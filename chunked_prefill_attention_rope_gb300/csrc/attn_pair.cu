@@ -67,6 +67,8 @@ constexpr int kSwitchCost = 3;
 // kernel; a plan that deals whole blocks is kept while its busiest team has at
 // most this many key tiles more than the even split's share.
 constexpr int kCutCost = 2 * kSwitchCost;
+// Whole-block deal: key tiles prefetched into L2 this far ahead of the copies.
+constexpr int kPrefetchTiles = 4;
 
 template <int D>
 struct PairCfg {
@@ -88,6 +90,7 @@ struct PairCfg {
 
 struct __align__(8) PairBars {
   uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t k_empty[4];  // whole-block deal: K stage free (its S = Q K done); kv_empty then frees V only
   uint64_t v_ready[4];  // implicit mask: V tile landed and its dead rows cleared (warp 11)
   uint64_t s_full[2], p_full[2], o_done[2], q_full[2], q_free[2];
   uint64_t mma_done;
@@ -611,6 +614,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_ready[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -667,7 +671,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         const TilePlan tp = block_plan(p, bx);
         for (int j = a; j < e; ++j, ++g) {
           const int st = g % NS;
-          if (!(ok = mbar_wait(&bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
+          if (!(ok = mbar_wait(PERM ? &bars->k_empty[st] : &bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
           // checked build's test hook: no copy for this tile, so that the
           // consumer's bounded wait for it runs out
           if (kTestHooks && g == p.test_drop_tile) continue;
@@ -680,10 +684,25 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
             tma_load_4d(sK + st * CF::kKBytes + blk * kBN * 128, mk, &bars->k_full[st], blk * 64, base, x.kvh, x.b);
+          if (PERM && !(ok = mbar_wait(&bars->kv_empty[st], ((g / NS) + 1) & 1, abort))) break;
           mbar_arrive_expect_tx(&bars->v_full[st], CF::kVBytes);
 #pragma unroll
           for (int blk = 0; blk < D / 64; ++blk)
             tma_load_4d(sV + st * CF::kVBytes + blk * kBN * 128, mv, &bars->v_full[st], blk * 64, base, x.kvh, x.b);
+          if (PERM) {
+            // Short segments whose tiles come cold from HBM: prefetch the
+            // segment's next tiles into L2 (a few tiles ahead of the copies)
+            for (int jp = (j == a ? j + 1 : j + kPrefetchTiles); jp <= j + kPrefetchTiles && jp < e; ++jp) {
+              const int t2 = tp.index(jp);
+              const bool chunk2 = t2 < tp.Tc;
+              const int base2 = (chunk2 ? t2 : t2 - tp.Tc) * kBN;
+#pragma unroll
+              for (int blk = 0; blk < D / 64; ++blk) {
+                tma_prefetch_4d(chunk2 ? &map_kn : &map_kc, blk * 64, base2, x.kvh, x.b);
+                tma_prefetch_4d(chunk2 ? &map_vn : &map_vc, blk * 64, base2, x.kvh, x.b);
+              }
+            }
+          }
         }
       }
       for (int j = max(0, g - NS); j < g; ++j) {  // let copies in flight land
@@ -755,6 +774,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         if (!(ok = warp_all(mbar_wait(&bars->q_full[1], seg & 1, abort)))) break;
         tc_fence_after();
         issue_qk(1, g);
+        if (PERM) commit(&bars->k_empty[g % NS]);
         for (int jj = 0; jj < n; ++jj) {
           const int gt = g + jj;
           const int st = gt % NS;
@@ -774,8 +794,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           tc_fence_after();
           issue_pv(1, gt, jj == 0);
           commit(&bars->kv_empty[st]);
-          if (jj + 1 == n) commit(&bars->o_done[1]);
-          else issue_qk(1, gt + 1);
+          if (jj + 1 == n) {
+            commit(&bars->o_done[1]);
+          } else {
+            issue_qk(1, gt + 1);
+            if (PERM) commit(&bars->k_empty[(gt + 1) % NS]);
+          }
         }
         g += n;
         ++seg;
