@@ -54,6 +54,7 @@ struct __align__(8) AttnBars {
   uint64_t p_full, pv_done, q_full, q_ready, mma_done;
   uint32_t tmem_base;
   int abort;
+  int sel;  // the caller's selected row of this sequence, read once at the start
 };
 
 template <int D, int BN>
@@ -113,8 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // combine_kernel (if any) may be scheduled now, except on a partial SM
   // budget (then as this grid ends); it waits for this grid
   if (!p.hold_dependents) grid_launch_dependents();
-  const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
-  const int my_nt = tp.count();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -133,19 +132,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
-    if (my_nt > 0) {
-      // raw Q rows of the G heads, head-major ({64, R, G, 1} boxes; rows past
-      // the chunk arrive as zeros); RoPE is applied in place below
-      prefetch_tensormap(&map_q);
-      mbar_arrive_expect_tx(&bars->q_full, static_cast<uint32_t>(D * p.R * p.G * 2));
+    // raw Q rows of the G heads, head-major ({64, R, G, 1} boxes; rows past
+    // the chunk arrive as zeros); RoPE is applied in place below
+    prefetch_tensormap(&map_q);
+    mbar_arrive_expect_tx(&bars->q_full, static_cast<uint32_t>(D * p.R * p.G * 2));
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_4d(smem + SM::kQ + blk * kBM * 128, &map_q, &bars->q_full, blk * 64, qt * p.R, kvh * p.G, b);
-    }
-    if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P) && kvh == 0 && blockIdx.x == 0)
-      set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
-    if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C) && kvh == 0 && blockIdx.x == 0)
-      set_err(p.err, CPA_EBIT_NREAL_GT_C);
+    for (int blk = 0; blk < D / 64; ++blk)
+      tma_load_4d(smem + SM::kQ + blk * kBM * 128, &map_q, &bars->q_full, blk * 64, qt * p.R, kvh * p.G, b);
+    // read now so that the epilogue does not wait on a global load
+    bars->sel = p.sel_row ? p.sel_row[b] : -1;
   }
   // Softmax threads: table values of their first Q items, loaded while the
   // barriers, tensor memory and the Q copy are being set up.  An item is one
@@ -153,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kQT = 4;  // items per thread whose tables are held at once
   const int q_items = p.R * (D / 16);
   RopeTab qtab[kQT];
-  if (warp >= 2 && my_nt > 0) {
+  if (warp >= 2) {
 #pragma unroll
     for (int u = 0; u < kQT; ++u) {
       const int item = (threadIdx.x - 64) + 128 * u;
@@ -179,6 +174,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + SM::kV;
   uint8_t* sP = smem + SM::kP;
 
+  // Until the wait below returns, the launches before this grid (a previous
+  // call's append, this call's key pre-pass) may still be running, so only
+  // the caller's inputs are read before it: the Q copy and its rotation.
+  if (warp >= 2) {
+    const int tid = threadIdx.x - 64;
+    // RoPE on the raw Q rows in shared memory (128-byte-swizzled K-major
+    // operand tile), item by item, every head of the group per item.
+    {
+      const int R = p.R;
+      bool qok = warp_all(mbar_wait(&bars->q_full, 0, abort));
+      for (int it0 = 0; qok && it0 < q_items; it0 += 128 * kQT) {
+#pragma unroll
+        for (int u = 0; u < kQT; ++u) {
+          const int item = it0 + tid + 128 * u;
+          const int il = item / (D / 16), kc = item % (D / 16);
+          if (item >= q_items || qt * R + il >= p.C) continue;
+          if (it0 > 0) {
+            const int ri = qt * R + il;
+            if (!in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) continue;
+            const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
+            const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
+            qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+          }
+          const int kh = kc + D / 16;
+          for (int g = 0; g < p.G; ++g) {
+            const int r = g * R + il;
+            uint4* pl = reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8));
+            uint4* ph = reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8));
+            uint4 lo = *pl, hi = *ph;
+            rope_apply<F16>(lo, hi, qtab[u]);
+            *pl = lo;
+            *ph = hi;
+          }
+        }
+      }
+      // rows past the G * R packed rows stay zero
+      for (int item = tid; item < (kBM - p.G * R) * (D / 8); item += 128) {
+        const int r = p.G * R + item / (D / 8);
+        const int c = item % (D / 8);
+        *reinterpret_cast<uint4*>(sQ + (c / 8) * (kBM * 128) + sw128(r, c % 8)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    fence_async_smem();
+    mbar_arrive(&bars->q_ready);
+  }
+  grid_dependency_wait();
+  if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) {
+    if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
+    if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  }
+  const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
+  const int my_nt = tp.count();
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && my_nt > 0) {
@@ -187,19 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&map_kn);
       prefetch_tensormap(&map_vn);
       int issued = 0;
-      bool waited_keys = false;
       for (int q = 0; q < my_nt; ++q) {
         const int st = q % kStages;
         if (!mbar_wait(&bars->kv_empty[st], ((q / kStages) + 1) & 1, abort)) break;
         const int j = tp.index(q);
         const bool chunk = j < tp.Tc;
         const int base = (chunk ? j : j - tp.Tc) * BN;
-        if ((chunk || p.app_n) && !waited_keys) {
-          // rotated chunk keys (and, with a fused append, new cache rows) are
-          // written by the preceding grid
-          grid_dependency_wait();
-          waited_keys = true;
-        }
         const CUtensorMap* mk = chunk ? &map_kn : &map_kc;
         const CUtensorMap* mv = chunk ? &map_vn : &map_vc;
         mbar_arrive_expect_tx(&bars->k_full[st], SM::kKBytes);
@@ -289,45 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = g < p.G && i < p.C;
     const int h = kvh * p.G + (valid ? g : 0);
 
-    // RoPE on the raw Q rows in shared memory (128-byte-swizzled K-major
-    // operand tile), item by item, every head of the group per item.
-    if (my_nt > 0) {
-      const int R = p.R;
-      bool qok = warp_all(mbar_wait(&bars->q_full, 0, abort));
-      for (int it0 = 0; qok && it0 < q_items; it0 += 128 * kQT) {
-#pragma unroll
-        for (int u = 0; u < kQT; ++u) {
-          const int item = it0 + tid + 128 * u;
-          const int il = item / (D / 16), kc = item % (D / 16);
-          if (item >= q_items || qt * R + il >= p.C) continue;
-          if (it0 > 0) {
-            const int ri = qt * R + il;
-            if (!in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) continue;
-            const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-            const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-            qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-          }
-          const int kh = kc + D / 16;
-          for (int g = 0; g < p.G; ++g) {
-            const int r = g * R + il;
-            uint4* pl = reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8));
-            uint4* ph = reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8));
-            uint4 lo = *pl, hi = *ph;
-            rope_apply<F16>(lo, hi, qtab[u]);
-            *pl = lo;
-            *ph = hi;
-          }
-        }
-      }
-      // rows past the G * R packed rows stay zero
-      for (int item = tid; item < (kBM - p.G * R) * (D / 8); item += 128) {
-        const int r = p.G * R + item / (D / 8);
-        const int c = item % (D / 8);
-        *reinterpret_cast<uint4*>(sQ + (c / 8) * (kBM * 128) + sw128(r, c % 8)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    fence_async_smem();
-    mbar_arrive(&bars->q_ready);
 
     // Visible key intervals of this row (implicit mask).
     const int W = p.window;
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (one split) or fp32 partials.  Row indices come from the table, four
       // rows per step.
       const int w = warp - 2;
-      const int sel = p.sel_row ? p.sel_row[b] : tp.n - 1;
+      const int sel = p.sel_row ? bars->sel : tp.n - 1;
       const size_t part_base = static_cast<size_t>(split) * p.B * p.Hq * p.C;
 #pragma unroll 4
       for (int k = 0; k < 32; ++k) {
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int S = p.splits;
       const int rows_per = kBM / S;
       const int w = warp - 2;
-      const int sel = p.sel_row ? p.sel_row[b] : tp.n - 1;
+      const int sel = p.sel_row ? bars->sel : tp.n - 1;
       const long long* tab_row = reinterpret_cast<const long long*>(smem + SM::kTabRow);
       const int* tab_i = reinterpret_cast<const int*>(smem + SM::kTabI);
       const int* tab_bh = reinterpret_cast<const int*>(smem + SM::kTabBh);
@@ -622,6 +624,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ls[s2] = s2 < S ? rlse[s2 * rows_per + j] : -INFINITY;
           lmax = fmaxf(lmax, ls[s2]);
         }
+        // Every split's chunks are loaded before any is used (the loads
+        // overlap); splits without live keys are skipped in the sums, which
+        // run in split order.
+        float4 part[kMaxClusterSplits][CPL];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+#pragma unroll
+          for (int q = 0; q < CPL; ++q) {
+            const int e = lane + 32 * q;
+            part[s2][q] = (s2 < S && lane < NCH)
+                              ? *reinterpret_cast<const float4*>(smem + 16u * ((s2 * NCH + e) * rows_per + (j ^ (e & 7))))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         float4 acc[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -634,13 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             wsum += wgt;
 #pragma unroll
             for (int q = 0; q < CPL; ++q) {
-              const int e = lane + 32 * q;
-              const float4 v = *reinterpret_cast<const float4*>(
-                  smem + 16u * ((s2 * NCH + e) * rows_per + (j ^ (e & 7))));
-              acc[q].x = __fmaf_rn(wgt, v.x, acc[q].x);
-              acc[q].y = __fmaf_rn(wgt, v.y, acc[q].y);
-              acc[q].z = __fmaf_rn(wgt, v.z, acc[q].z);
-              acc[q].w = __fmaf_rn(wgt, v.w, acc[q].w);
+              acc[q].x = __fmaf_rn(wgt, part[s2][q].x, acc[q].x);
+              acc[q].y = __fmaf_rn(wgt, part[s2][q].y, acc[q].y);
+              acc[q].z = __fmaf_rn(wgt, part[s2][q].z, acc[q].z);
+              acc[q].w = __fmaf_rn(wgt, part[s2][q].w, acc[q].w);
             }
           }
         }
@@ -665,17 +677,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // This grid completes only after the key pre-pass has (stream order for
-  // whatever follows).
-  if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 // Rotated chunk keys for the single-tile kernel: one thread per (row, 8-dim
 // chunk pair), the append's fp32 arithmetic.  It lets the dependent attention
 // grid start at once.
 __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
-  grid_launch_dependents();
-  grid_dependency_wait();  // launched as a dependent: whatever the launches before it wrote
+  grid_launch_dependents();  // the attention grid starts now; it waits for this grid before using lengths or keys
+  grid_dependency_wait();    // launched as a dependent: whatever the launches before it wrote
   const int D = p.D;
   const int HP = D / 16;
   const int sh = __ffs(HP) - 1;  // HP is a power of two

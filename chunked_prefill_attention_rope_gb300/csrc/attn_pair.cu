@@ -235,8 +235,15 @@ constexpr int kPrepHeads = 4;  // heads rotated per item with one table load (tw
 constexpr int kPlanSortMax = 1024;
 
 // Key tiles of block u plus the switch cost (0 for a block without live tiles).
+// The first block of each sequence also checks the sequence's lengths, which
+// the plan loads here anyway.
 __device__ __forceinline__ int block_cost(const AttnParams& p, int u) {
-  const int n = block_plan(p, block_of(p, u)).count();
+  const Block x = block_of(p, u);
+  if (x.kvh == 0 && x.blk == 0) {
+    if (p.past_len && (p.past_len[x.b] < 0 || p.past_len[x.b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
+    if (p.n_real && (p.n_real[x.b] < 0 || p.n_real[x.b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  }
+  const int n = block_plan(p, x).count();
   return n > 0 ? n + kSwitchCost : 0;
 }
 
@@ -491,6 +498,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const AttnParams 
   if (blockIdx.x == 0) {  // the first CTA to start plans, alongside the rotations
     if (p.mask) explicit_hulls(p);
     plan_units(p);
+    // and marks the attention's partial-result slots empty (it reads them
+    // only after waiting for this grid)
+    for (int k = threadIdx.x; k < 2 * p.ctas; k += blockDim.x) st_chk(p.ptag, k, 2LL * p.ctas, -1, p.err);
     return;
   }
   const int D = p.D;
@@ -627,14 +637,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
-    st_chk(p.ptag, 2 * cta, 2LL * p.ctas, -1, p.err);  // no partial result of this call yet
-    st_chk(p.ptag, 2 * cta + 1, 2LL * p.ctas, -1, p.err);
-    if (cta == 0) {
-      for (int b = 0; b < p.B; ++b) {
-        if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
-        if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
-      }
-    }
   }
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -645,6 +647,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   // grid ends, leaving the other SMs to other streams); this grid's inputs
   // (plan, rotated Q and keys) come from prep_kernel, launched just before it
   if (!p.hold_dependents) grid_launch_dependents();
+  // Global memory only after this wait: until it returns, launches before the
+  // one just ahead of this grid (a previous call's work on the same
+  // workspace or cache) may still be running.
   grid_dependency_wait();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
