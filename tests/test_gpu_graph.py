@@ -109,3 +109,78 @@ def test_page1_eighteen_layers_as_one_cuda_graph():
                                    ctx["L"], ctx["n"], mask=sh["mask"], sel_row=sel)
         assert_close(ly["out"], ref, f"page1 graph/L{l}")
         check_argmax(ly["sel"], ref_sel, f"page1 graph/L{l}")
+
+
+@pytest.mark.parametrize("D,window", [(256, 0), (256, 96), (128, 0)])
+def test_chunk_sequence_in_one_graph_reads_each_previous_append(D, window):
+    """Chunked prefill as one CUDA graph: four chunks, each an attention call
+    whose past length is the cache's own length, then the chunk's append.  In
+    a graph the launches follow one another with no host gap, so every chunk
+    must see exactly the rows and length the previous chunk's append wrote
+    ("functiongemma: chunk prefill-with-past graph", Change: K/V extended by
+    the chunk).  Each chunk's output is checked against the oracle run chunk
+    by chunk, and the final cache bytes and lengths exactly."""
+    import oracle as O
+    from synth import normal_bf16, bf16_bits
+    from harness import bits16
+    cpa = lib()
+    B, Hq, Hkv, C, NCH = 2, 8, 2, 64, 4
+    L0 = np.array([37, 100])
+    cap = int(L0.max()) + NCH * C
+    ck = normal_bf16((B, Hkv, cap, D), 0, f"seqgraph/{D}/ck")
+    cv = normal_bf16((B, Hkv, cap, D), 0, f"seqgraph/{D}/cv")
+    chunks = []
+    for c in range(NCH):
+        pos = L0[:, None] + c * C + np.arange(C)[None, :]
+        cos, sin = rope_tables(pos, D, 10000.0)
+        chunks.append(dict(q=normal_bf16((B, Hq, C, D), 0, f"seqgraph/{D}/{c}/q"),
+                           k=normal_bf16((B, Hkv, C, D), 0, f"seqgraph/{D}/{c}/k"),
+                           v=normal_bf16((B, Hkv, C, D), 0, f"seqgraph/{D}/{c}/v"), cos=cos, sin=sin))
+    dev = [{k: t.to(DEV) for k, t in ch.items()} for ch in chunks]
+    full = torch.full((B,), C, dtype=torch.int32, device=DEV)
+    cache = cpa.KVCache(ck.to(DEV), cv.to(DEV), torch.from_numpy(L0.astype(np.int32)).to(DEV))
+    outs = [torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=DEV) for _ in range(NCH)]
+    ws = torch.empty(max(1, cpa.attn_workspace_size(B, Hq, Hkv, D, C, cap)), dtype=torch.uint8, device=DEV)
+    err = cpa.new_error_word()
+
+    def run():
+        for c in range(NCH):
+            x = dev[c]
+            cpa.chunk_prefill_attn(x["q"], x["k"], x["v"], x["cos"], x["sin"], cache, cap, past_len=cache.len,
+                                   n_real=full, window=window, out=outs[c], workspace=ws, err=err)
+            cpa.kv_append(cache, x["k"], x["v"], x["cos"], x["sin"], full, err=err)
+
+    def reset():
+        cache.k.copy_(ck.to(DEV))
+        cache.v.copy_(cv.to(DEV))
+        cache.len.copy_(torch.from_numpy(L0.astype(np.int32)).to(DEV))
+
+    run()                                   # eager warm-up (kernel attributes before capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    reset()
+    with torch.cuda.graph(g):
+        run()
+    # the oracle, chunk by chunk over its own copy of the cache
+    ok_, ov_ = bits16(ck).copy(), bits16(cv).copy()
+    olen = L0.astype(np.int64).copy()
+    refs = []
+    for c in range(NCH):
+        x = chunks[c]
+        ref, _ = O.chunk_prefill_attn(bf16_bits(x["q"]), bf16_bits(x["k"]), bf16_bits(x["v"]), x["cos"].numpy(),
+                                      x["sin"].numpy(), ok_, ov_, cap, olen.copy(), np.full(B, C), window=window,
+                                      causal=1)
+        refs.append(ref)
+        assert O.kv_append_global(ok_, ov_, olen, bf16_bits(x["k"]), bf16_bits(x["v"]), x["cos"].numpy(),
+                                  x["sin"].numpy(), np.full(B, C)) == []
+    for rep in range(3):
+        reset()
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err[0]) == 0
+        for c in range(NCH):
+            assert_close(outs[c], refs[c], f"chunk graph D{D} w{window} rep{rep} chunk{c}")
+        assert cache.len.cpu().numpy().tolist() == olen.tolist()
+        assert np.array_equal(bits16(cache.k), ok_) and np.array_equal(bits16(cache.v), ov_)
