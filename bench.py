@@ -51,9 +51,9 @@ KERNEL_SOURCES = {
 }
 MEASURED_TRAFFIC = {
     # long-context chunk call: prep + attn_pair + merge, one ncu capture of the second call
-    "prefill": {"src": "f807a3885f57611a", "bytes": 644500000},
-    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0069 x)
-    "decode": {"src": "1a2b2990ced6f654", "bytes": 4829108015},
+    "prefill": {"src": "a9d77a1d9a17f725", "bytes": 644325376},
+    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0071 x)
+    "decode": {"src": "960cdf5e090c4d75", "bytes": 4830099533},
 }
 
 def source_hash(kind):
