@@ -28,6 +28,7 @@ __all__ = [
     "CpaError", "KVCache", "load_library", "lib_path", "using_library", "chunk_prefill_attn", "chunk_prefill_attn_noalloc",
     "decode_step", "chunk_prefill_attn_append",
     "kv_append", "kv_snapshot_padded_append", "kv_rollback_padded_append",
+    "PreparedCall", "prepare_chunk_prefill_attn", "prepare_chunk_prefill_attn_append", "prepare_kv_append",
     "attn_workspace_size", "attn_workspace_size_mask", "cache_scratch_size", "new_error_word", "EBIT", "GLOBAL", "SLIDING",
     "tail_plan", "TAIL_SCALAR", "TAIL_PADDED", "TAIL_AUTO", "TAIL_FORCE_SCALAR", "TAIL_FORCE_PADDED",
 ]
@@ -201,10 +202,29 @@ def cache_scratch_size(cache: KVCache, C: int) -> int:
     return int(load_library().cpa_cache_scratch_size(cache._ref, cache.B, cache.Hkv, cache.D, C))
 
 
-def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
-          window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
-          out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None, stream=None,
-          alloc_workspace: bool = True, append_rows=None, sm_budget: int = 0):
+class PreparedCall:
+    """One library call whose arguments were checked and marshalled once.
+    Calling it enqueues the call again on the same tensors, whose contents may
+    change between calls but which must stay where they are; it returns the
+    call's outputs.  For drivers that keep their buffers in place (a model's
+    layer loop run eagerly): a call then costs the C entry point alone."""
+
+    __slots__ = ("_fn", "_args", "_dev", "_keep", "outputs")
+
+    def __init__(self, fn, args, dev, keep, outputs):
+        self._fn, self._args, self._dev, self._keep, self.outputs = fn, args, dev, keep, outputs
+
+    def __call__(self, stream=None):
+        _check(self._fn(*self._args, _stream(stream, self._dev)))
+        return self.outputs
+
+
+def _attn_build(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_len=None, n_real=None,
+                window: int = 0, causal: bool = True, mask=None, scale: float = 0.0, sel_row=None,
+                out=None, out_sel=None, want_sel: bool = False, workspace=None, err=None,
+                alloc_workspace: bool = True, append_rows=None, sm_budget: int = 0):
+    """Checks the arguments of an attention entry point and marshals them:
+    (function, leading C arguments, device, tensors to keep alive, outputs)."""
     lib = load_library()
     B, Hq, C, D = q.shape
     Hkv = k_new.shape[1]
@@ -245,12 +265,31 @@ def _attn(entry: str, q, k_new, v_new, cos, sin, cache: KVCache, P: int, past_le
                   None if out_sel is None else out_sel.data_ptr(),
                   None if workspace is None else workspace.data_ptr(),
                   0 if workspace is None else workspace.numel(), err.data_ptr(), int(sm_budget))
+    args = (ctypes.byref(a),)
     if append_rows is not None:
         _need(append_rows, "n_rows", i32, row_shape)
-        _check(getattr(lib, entry)(ctypes.byref(a), append_rows.data_ptr(), _stream(stream, dev)))
-    else:
-        _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream, dev)))
-    return out, out_sel
+        args = (ctypes.byref(a), append_rows.data_ptr())
+    keep = (a, cache, q, k_new, v_new, cos, sin, mask, past_len, n_real, sel_row, workspace, err, append_rows)
+    return getattr(lib, entry), args, dev, keep, (out, out_sel)
+
+
+def _attn(entry: str, *a, stream=None, **kw):
+    fn, args, dev, _keep, outs = _attn_build(entry, *a, **kw)
+    _check(fn(*args, _stream(stream, dev)))
+    return outs
+
+
+def prepare_chunk_prefill_attn(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw) -> PreparedCall:
+    """chunk_prefill_attn with its arguments bound once: calling the result
+    runs the call again and returns (out, out_sel)."""
+    return PreparedCall(*_attn_build("cpa_chunk_prefill_attn", q, k_new, v_new, cos, sin, cache, P, **kw))
+
+
+def prepare_chunk_prefill_attn_append(q, k_new, v_new, cos, sin, cache: KVCache, P: int, n_rows,
+                                      **kw) -> PreparedCall:
+    """chunk_prefill_attn_append with its arguments bound once."""
+    return PreparedCall(*_attn_build("cpa_chunk_prefill_attn_append", q, k_new, v_new, cos, sin, cache, P,
+                                     append_rows=n_rows, **kw))
 
 
 def chunk_prefill_attn(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
@@ -284,6 +323,18 @@ def decode_step(q, k_new, v_new, cos, sin, cache: KVCache, P: int, **kw):
 
 def kv_append(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch=None, err=None, stream=None):
     """Append rows [0, n_rows[b]) of the chunk (K rotated, V copied) to the cache."""
+    fn, args, dev, _keep, err = _append_build(cache, k_new, v_new, cos, sin, n_rows, scratch, err)
+    _check(fn(*args, _stream(stream, dev)))
+    return err
+
+
+def prepare_kv_append(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch=None, err=None) -> PreparedCall:
+    """kv_append with its arguments bound once: calling the result runs the
+    append again (the cache's length advances each time) and returns err."""
+    return PreparedCall(*_append_build(cache, k_new, v_new, cos, sin, n_rows, scratch, err))
+
+
+def _append_build(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch, err):
     lib = load_library()
     B, Hkv, C, D = k_new.shape
     kv_shape, tab_shape = (B, Hkv, C, D), (B, C, D)
@@ -297,11 +348,10 @@ def kv_append(cache: KVCache, k_new, v_new, cos, sin, n_rows, scratch=None, err=
         err = new_error_word(dev)
     if scratch is None and cache.kind == SLIDING:
         scratch = torch.empty(cache_scratch_size(cache, C), dtype=torch.uint8, device=dev)
-    _check(lib.cpa_kv_append(cache._ref, k_new.data_ptr(), v_new.data_ptr(), cos.data_ptr(),
-                             sin.data_ptr(), n_rows.data_ptr(), B, Hkv, D, C,
-                             None if scratch is None else scratch.data_ptr(),
-                             0 if scratch is None else scratch.numel(), err.data_ptr(), _stream(stream, dev)))
-    return err
+    args = (cache._ref, k_new.data_ptr(), v_new.data_ptr(), cos.data_ptr(), sin.data_ptr(), n_rows.data_ptr(),
+            B, Hkv, D, C, None if scratch is None else scratch.data_ptr(), 0 if scratch is None else scratch.numel(),
+            err.data_ptr())
+    return lib.cpa_kv_append, args, dev, (cache, k_new, v_new, cos, sin, n_rows, scratch, err), err
 
 
 def kv_snapshot_padded_append(cache: KVCache, n_real, C: int, scratch, err=None, stream=None):

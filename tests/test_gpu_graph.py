@@ -184,3 +184,39 @@ def test_chunk_sequence_in_one_graph_reads_each_previous_append(D, window):
             assert_close(outs[c], refs[c], f"chunk graph D{D} w{window} rep{rep} chunk{c}")
         assert cache.len.cpu().numpy().tolist() == olen.tolist()
         assert np.array_equal(bits16(cache.k), ok_) and np.array_equal(bits16(cache.v), ov_)
+
+
+def test_prepared_calls_equal_plain_calls():
+    """The page-1 layers run eagerly through prepared calls (arguments bound
+    once, then only enqueued) give the same bits as the plain binding:
+    outputs, selected rows, cache bytes and lengths."""
+    cpa = lib()
+    ctx, layers = build_layers(cpa)
+    reset(layers, ctx)
+    run_layers(cpa, ctx, layers)
+    torch.cuda.synchronize()
+    plain = snapshot(layers)
+    w = ctx["w"]
+    calls = []
+    for ly in layers:
+        sh = ctx["dshared"][ly["kind"]]
+        calls.append(cpa.prepare_chunk_prefill_attn(
+            ly["q"], ly["k"], ly["v"], sh["cos"], sh["sin"], ly["cache"], w.P, past_len=ctx["past"],
+            n_real=ctx["n_real"], mask=sh["mask"], sel_row=ctx["sel_row"], out=ly["out"], out_sel=ly["sel"],
+            workspace=ctx["ws"], err=ctx["err"]))
+        calls.append(cpa.prepare_kv_append(ly["cache"], ly["k"], ly["v"], sh["cos"], sh["sin"], ctx["n_real"],
+                                           err=ctx["err"]))
+    for rep in range(2):
+        reset(layers, ctx)
+        for ly in layers:
+            ly["out"].zero_()
+            ly["sel"].zero_()
+        for call in calls:
+            call()
+        torch.cuda.synchronize()
+        assert int(ctx["err"][0]) == 0
+        for l, (ly, e) in enumerate(zip(layers, plain)):
+            got = (ly["out"], ly["sel"], ly["cache"].k, ly["cache"].v, ly["cache"].len)
+            for name, a, b in zip(("out", "sel", "k", "v", "len"), got, e):
+                assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                                   b.view(torch.uint8) if b.dtype != torch.int32 else b), (rep, l, name)
