@@ -124,7 +124,7 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0
 // Workspace of the decode and single-tile paths: split-KV partials (when
 // combine_kernel merges them), then the rotated chunk keys (single-tile path).
 struct SingleWorkspace {
-  size_t part_o, part_lse, k_rot, v_cvt, total;
+  size_t part_o, part_lse, q_rot, k_rot, v_cvt, total;
 };
 SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int D, int C) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -138,6 +138,8 @@ SingleWorkspace single_workspace(const Geometry& g, int B, int Hq, int Hkv, int 
     off += al(static_cast<size_t>(g.splits) * rows * sizeof(float));
   }
   if (g.path == kPathSingle) {
+    w.q_rot = off;  // the rotated queries (in half for an fp16 cache)
+    off += al(static_cast<size_t>(B) * Hq * C * D * 2);
     w.k_rot = off;
     off += al(static_cast<size_t>(B) * Hkv * C * D * 2);
     w.v_cvt = off;  // fp16 cache: the chunk values in half
@@ -325,10 +327,11 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
     p.n_part = static_cast<long long>(g.splits) * a->B * a->Hq * a->C * a->D;
   }
   if (g.path == kPathSingle) {
-    // raw Q rows (box {64, R, G, 1}); chunk keys from the rotated copy
+    // Q rows and chunk keys from the pre-pass's rotated copies (Q box {64, R, G, 1})
+    p.q_rot = reinterpret_cast<uint16_t*>(w + L.q_rot);
     p.k_rot = reinterpret_cast<uint16_t*>(w + L.k_rot);
     p.v_cvt = reinterpret_cast<uint16_t*>(w + L.v_cvt);
-    if (!make_map(&maps[4], a->q, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G) ||
+    if (!make_map(&maps[4], p.q_rot, a->D, a->C, a->Hq, a->B, a->D, cs_, cs_ * a->Hq, g.R, g.G) ||
         !make_map(&maps[2], p.k_rot, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn) ||
         (p.f16 && !make_map(&maps[3], p.v_cvt, a->D, a->C, a->Hkv, a->B, a->D, cs_, cs_ * a->Hkv, bn)))
       return CPA_ERR_CUDA;

@@ -23,9 +23,9 @@
 //
 // Chunk keys: rope_chunk_k_kernel rotates them once per call into the
 // workspace (the append's arithmetic).  The attention grid is launched as a
-// programmatic dependent of it, so its prologue and Q rotation run while the
-// keys are rotated; the producer waits for that grid only before its first
-// chunk-key copy.
+// programmatic dependent of it, so its prologue and the Q copy and rotation
+// run while the keys are rotated; it then waits for that grid before it plans
+// from the lengths or reads any cached row.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: K and V tiles into a 2-stage shared-memory ring.
@@ -51,7 +51,7 @@ constexpr int kThreads = 192;
 struct __align__(8) AttnBars {
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, pv_done, q_full, q_ready, mma_done;
+  uint64_t p_full, pv_done, q_full, mma_done;
   uint32_t tmem_base;
   int abort;
   int sel;  // the caller's selected row of this sequence, read once at the start
@@ -128,39 +128,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->p_full, 128);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_ready, 128);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
-    // raw Q rows of the G heads, head-major ({64, R, G, 1} boxes; rows past
-    // the chunk arrive as zeros); RoPE is applied in place below
     prefetch_tensormap(&map_q);
-    mbar_arrive_expect_tx(&bars->q_full, static_cast<uint32_t>(D * p.R * p.G * 2));
-#pragma unroll
-    for (int blk = 0; blk < D / 64; ++blk)
-      tma_load_4d(smem + SM::kQ + blk * kBM * 128, &map_q, &bars->q_full, blk * 64, qt * p.R, kvh * p.G, b);
-    // read now so that the epilogue does not wait on a global load
-    bars->sel = p.sel_row ? p.sel_row[b] : -1;
   }
-  // Softmax threads: table values of their first Q items, loaded while the
-  // barriers, tensor memory and the Q copy are being set up.  An item is one
-  // (chunk row, 8-dim chunk pair); its table values serve all G heads.
-  constexpr int kQT = 4;  // items per thread whose tables are held at once
-  const int q_items = p.R * (D / 16);
-  RopeTab qtab[kQT];
-  if (warp >= 2) {
-#pragma unroll
-    for (int u = 0; u < kQT; ++u) {
-      const int item = (threadIdx.x - 64) + 128 * u;
-      const int il = item / (D / 16), kc = item % (D / 16);
-      const int ri = qt * p.R + il;
-      if (item < q_items && ri < p.C && in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) {
-        const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-        const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-        qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-      }
-    }
+  // The Q tile's rows past the G * R packed rows, which the Q copy does not
+  // write, stay zero.
+  for (int item = threadIdx.x; item < (kBM - p.G * p.R) * (D / 8); item += kThreads) {
+    const int r = p.G * p.R + item / (D / 8);
+    const int c = item % (D / 8);
+    *reinterpret_cast<uint4*>(smem + SM::kQ + (c / 8) * (kBM * 128) + sw128(r, c % 8)) = make_uint4(0, 0, 0, 0);
   }
+  fence_async_smem();
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
@@ -174,55 +154,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + SM::kV;
   uint8_t* sP = smem + SM::kP;
 
-  // Until the wait below returns, the launches before this grid (a previous
-  // call's append, this call's key pre-pass) may still be running, so only
-  // the caller's inputs are read before it: the Q copy and its rotation.
-  if (warp >= 2) {
-    const int tid = threadIdx.x - 64;
-    // RoPE on the raw Q rows in shared memory (128-byte-swizzled K-major
-    // operand tile), item by item, every head of the group per item.
-    {
-      const int R = p.R;
-      bool qok = warp_all(mbar_wait(&bars->q_full, 0, abort));
-      for (int it0 = 0; qok && it0 < q_items; it0 += 128 * kQT) {
-#pragma unroll
-        for (int u = 0; u < kQT; ++u) {
-          const int item = it0 + tid + 128 * u;
-          const int il = item / (D / 16), kc = item % (D / 16);
-          if (item >= q_items || qt * R + il >= p.C) continue;
-          if (it0 > 0) {
-            const int ri = qt * R + il;
-            if (!in_bounds((static_cast<long long>(b) * p.C + ri) * D, D, n_tab(p), p.err)) continue;
-            const float* cr = p.cos + (static_cast<size_t>(b) * p.C + ri) * D;
-            const float* sr = p.sin + (static_cast<size_t>(b) * p.C + ri) * D;
-            qtab[u] = rope_tab(cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
-          }
-          const int kh = kc + D / 16;
-          for (int g = 0; g < p.G; ++g) {
-            const int r = g * R + il;
-            uint4* pl = reinterpret_cast<uint4*>(sQ + (kc / 8) * (kBM * 128) + sw128(r, kc % 8));
-            uint4* ph = reinterpret_cast<uint4*>(sQ + (kh / 8) * (kBM * 128) + sw128(r, kh % 8));
-            uint4 lo = *pl, hi = *ph;
-            rope_apply<F16>(lo, hi, qtab[u]);
-            *pl = lo;
-            *ph = hi;
-          }
-        }
-      }
-      // rows past the G * R packed rows stay zero
-      for (int item = tid; item < (kBM - p.G * R) * (D / 8); item += 128) {
-        const int r = p.G * R + item / (D / 8);
-        const int c = item % (D / 8);
-        *reinterpret_cast<uint4*>(sQ + (c / 8) * (kBM * 128) + sw128(r, c % 8)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    fence_async_smem();
-    mbar_arrive(&bars->q_ready);
-  }
+  // Nothing of the call's or the caller's memory is touched before this wait:
+  // until it returns, the key pre-pass (which also rotates the queries) and,
+  // through it, earlier launches may still be running.
   grid_dependency_wait();
-  if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) {
-    if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
-    if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+  if (threadIdx.x == 0) {
+    // the rotated Q rows of the G heads, head-major ({64, R, G, 1} boxes;
+    // rows past the chunk arrive as zeros)
+    mbar_arrive_expect_tx(&bars->q_full, static_cast<uint32_t>(D * p.R * p.G * 2));
+#pragma unroll
+    for (int blk = 0; blk < D / 64; ++blk)
+      tma_load_4d(smem + SM::kQ + blk * kBM * 128, &map_q, &bars->q_full, blk * 64, qt * p.R, kvh * p.G, b);
+    bars->sel = p.sel_row ? p.sel_row[b] : -1;
+    if (kvh == 0 && blockIdx.x == 0) {
+      if (p.past_len && (p.past_len[b] < 0 || p.past_len[b] > p.P)) set_err(p.err, CPA_EBIT_PAST_GT_SPAN);
+      if (p.n_real && (p.n_real[b] < 0 || p.n_real[b] > p.C)) set_err(p.err, CPA_EBIT_NREAL_GT_C);
+    }
   }
   const TilePlan tp = plan_tiles<BN>(p, b, qt * p.R, min(qt * p.R + p.R, p.C) - 1, split);
   const int my_nt = tp.count();
@@ -271,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_16(kBM, D, true, F16);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t p_addr = smem_u32(sP);
-      bool ok = my_nt > 0 ? warp_all(mbar_wait(&bars->q_ready, 0, abort)) : true;
+      bool ok = my_nt > 0 ? warp_all(mbar_wait(&bars->q_full, 0, abort)) : true;
       auto issue_pv = [&](int q) -> bool {
         const int st = q % kStages;
         if (!warp_all(mbar_wait(&bars->p_full, q & 1, abort))) return false;
@@ -683,13 +630,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chunk pair), the append's fp32 arithmetic.  It lets the dependent attention
 // grid start at once.
 __global__ void __launch_bounds__(256) rope_chunk_k_kernel(const AttnParams p) {
-  grid_launch_dependents();  // the attention grid starts now; it waits for this grid before using lengths or keys
+  grid_launch_dependents();  // the attention grid touches no memory before its own wait
   grid_dependency_wait();    // launched as a dependent: whatever the launches before it wrote
   const int D = p.D;
   const int HP = D / 16;
   const int sh = __ffs(HP) - 1;  // HP is a power of two
-  const unsigned total = static_cast<unsigned>(p.B) * p.Hkv * p.C * HP;  // < 2^31 (host)
+  const unsigned k_items = static_cast<unsigned>(p.B) * p.Hkv * p.C * HP;
+  const unsigned total = k_items + static_cast<unsigned>(p.B) * p.Hq * p.C * HP;  // < 2^31 (host)
   for (unsigned it = blockIdx.x * 256u + threadIdx.x; it < total; it += gridDim.x * 256u) {
+    if (it >= k_items) {
+      // a query row's chunk pair, rotated into the workspace (in half for an
+      // fp16 cache: the products then run in fp16)
+      const unsigned qi = it - k_items;
+      const int kc = static_cast<int>(qi & (HP - 1));
+      const unsigned qr = qi >> sh;  // row of [B, Hq, C]
+      const long long r = qr;
+      const int i = static_cast<int>(qr % static_cast<unsigned>(p.C));
+      const int b = static_cast<int>(qr / static_cast<unsigned>(p.C) / static_cast<unsigned>(p.Hq));
+      if (!in_bounds(r * D, D, n_qo(p), p.err) ||
+          !in_bounds((static_cast<long long>(b) * p.C + i) * D, D, n_tab(p), p.err))
+        continue;
+      const uint16_t* src = p.q + r * D;
+      uint4 lo = __ldg(reinterpret_cast<const uint4*>(src + kc * 8));
+      uint4 hi = __ldg(reinterpret_cast<const uint4*>(src + D / 2 + kc * 8));
+      const float* cr = p.cos + (static_cast<size_t>(b) * p.C + i) * D;
+      const float* sr = p.sin + (static_cast<size_t>(b) * p.C + i) * D;
+      if (p.f16) rope_pair<true>(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+      else rope_pair(lo, hi, cr + kc * 8, sr + kc * 8, cr + D / 2 + kc * 8, sr + D / 2 + kc * 8);
+      uint16_t* dst = p.q_rot + r * D;
+      *reinterpret_cast<uint4*>(dst + kc * 8) = lo;
+      *reinterpret_cast<uint4*>(dst + D / 2 + kc * 8) = hi;
+      continue;
+    }
     const int kc = static_cast<int>(it & (HP - 1));
     const unsigned rr = it >> sh;  // row of [B, Hkv, C]
     const long long r = rr;
@@ -814,7 +786,7 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   static SmemAttr smem_attr;
   if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), SM::kAlloc); e != cudaSuccess) return e;
   dim3 grid(p.nq * p.splits, p.Hkv, p.B);
-  const long long items = static_cast<long long>(p.B) * p.Hkv * p.C * (D / 16);
+  const long long items = static_cast<long long>(p.B) * (p.Hkv + p.Hq) * p.C * (D / 16);
   const int kblocks = static_cast<int>(max(1LL, min(static_cast<long long>(152) * 8, (items + 255) / 256)));
   cudaError_t e = launch_dependent(rope_chunk_k_kernel, dim3(kblocks), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;

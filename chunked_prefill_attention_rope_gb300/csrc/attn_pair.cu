@@ -734,6 +734,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       auto k_ready = [&](const TilePlan&, int, int gg) -> bool {
         return warp_all(mbar_wait(&bars->k_full[gg % NS], (gg / NS) & 1, abort));
       };
+      // Descriptors are formed once; the MMAs of a group step through them by
+      // constant offsets (the start-address field is address / 16).
       const uint64_t qd0 = sdesc_sw128(q_addr, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vd0 = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);

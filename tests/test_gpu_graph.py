@@ -220,3 +220,71 @@ def test_prepared_calls_equal_plain_calls():
             for name, a, b in zip(("out", "sel", "k", "v", "len"), got, e):
                 assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
                                    b.view(torch.uint8) if b.dtype != torch.int32 else b), (rep, l, name)
+
+
+@pytest.mark.parametrize("D,window", [(256, 0), (256, 96), (128, 0)])
+def test_outputs_fed_back_as_queries_in_one_graph(D, window):
+    """Each chunk's query is the previous chunk's output tensor, with the
+    appends in between, all captured in one CUDA graph: every call must read
+    what the call before it wrote, with no host gap between the launches.
+    The replays equal a run with a device sync after every call, bit for
+    bit; the first chunk (all inputs synthetic) also matches the oracle."""
+    from synth import normal_bf16
+    cpa = lib()
+    B, Hq, Hkv, C, NCH = 2, 8, 2, 64, 4
+    L0 = np.array([37, 100])
+    cap = int(L0.max()) + NCH * C
+    ck = normal_bf16((B, Hkv, cap, D), 0, f"fedback/{D}/ck")
+    cv = normal_bf16((B, Hkv, cap, D), 0, f"fedback/{D}/cv")
+    q0 = normal_bf16((B, Hq, C, D), 0, f"fedback/{D}/q0")
+    ks = [normal_bf16((B, Hkv, C, D), 0, f"fedback/{D}/{c}/k").to(DEV) for c in range(NCH)]
+    vs = [normal_bf16((B, Hkv, C, D), 0, f"fedback/{D}/{c}/v").to(DEV) for c in range(NCH)]
+    tabs = [tuple(t.to(DEV) for t in rope_tables(L0[:, None] + c * C + np.arange(C)[None, :], D, 10000.0))
+            for c in range(NCH)]
+    full = torch.full((B,), C, dtype=torch.int32, device=DEV)
+    cache = cpa.KVCache(ck.to(DEV), cv.to(DEV), torch.from_numpy(L0.astype(np.int32)).to(DEV))
+    qin = q0.to(DEV)
+    outs = [torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=DEV) for _ in range(NCH)]
+    ws = torch.empty(max(1, cpa.attn_workspace_size(B, Hq, Hkv, D, C, cap)), dtype=torch.uint8, device=DEV)
+    err = cpa.new_error_word()
+
+    def run(sync):
+        for c in range(NCH):
+            q = qin if c == 0 else outs[c - 1]
+            cos, sin = tabs[c]
+            cpa.chunk_prefill_attn(q, ks[c], vs[c], cos, sin, cache, cap, past_len=cache.len, n_real=full,
+                                   window=window, out=outs[c], workspace=ws, err=err)
+            if sync:
+                torch.cuda.synchronize()
+            cpa.kv_append(cache, ks[c], vs[c], cos, sin, full, err=err)
+            if sync:
+                torch.cuda.synchronize()
+
+    def reset():
+        cache.k.copy_(ck.to(DEV))
+        cache.v.copy_(cv.to(DEV))
+        cache.len.copy_(torch.from_numpy(L0.astype(np.int32)).to(DEV))
+        for o in outs:
+            o.zero_()
+
+    reset()
+    run(sync=True)
+    assert int(err[0]) == 0
+    ref = [o.clone() for o in outs] + [cache.k.clone(), cache.v.clone(), cache.len.clone()]
+    cos0, sin0 = (t.cpu() for t in tabs[0])
+    oref, _ = oracle_attn(q0, ks[0].cpu(), vs[0].cpu(), cos0, sin0, ck, cv, cap,
+                          torch.from_numpy(L0.astype(np.int32)), torch.full((B,), C, dtype=torch.int32), window, 1)
+    assert_close(outs[0], oref, f"fed back D{D} w{window} chunk 0")
+    g = torch.cuda.CUDAGraph()
+    reset()
+    with torch.cuda.graph(g):
+        run(sync=False)
+    for rep in range(3):
+        reset()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err[0]) == 0
+        got = outs + [cache.k, cache.v, cache.len]
+        for k, (a, b) in enumerate(zip(got, ref)):
+            assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                               b.view(torch.uint8) if b.dtype != torch.int32 else b), (rep, k)
