@@ -77,6 +77,7 @@ enum Path { kPathSingle = 0, kPathPair = 1, kPathDecode = 2 };
 struct Geometry {
   int G, R, nq, splits, path;
   bool cluster;  // single-tile splits merged inside a thread-block cluster
+  int dsplit;    // CTAs per split in that cluster (2: they divide D)
   PairTeams teams;
 };
 
@@ -96,6 +97,7 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0
   g.nq = (C + g.R - 1) / g.R;
   g.teams = PairTeams{};
   g.cluster = false;
+  g.dsplit = 1;
   const int dev_sms = num_sms();
   const int sms = sm_budget > 0 && sm_budget < dev_sms ? sm_budget : dev_sms;
   if (attn_uses_pair(D, g.nq) && !attn_uses_decode(D, C, g.G)) {
@@ -118,6 +120,10 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0
   g.splits = max(1, min(s, max(1, max_tiles)));
   g.cluster = g.path == kPathSingle && (g.splits == 2 || g.splits == 4 || g.splits == 8) &&
               attn_cluster_ok(D, g.splits);
+  // D = 256 over 8 splits: the merge's exchange of 128 KB of fp32 rows per CTA
+  // through distributed shared memory bounds the call, so each split is taken
+  // by two CTAs that divide D (each sends half), in clusters of 16
+  if (g.cluster && g.splits == 8 && D == 256 && ctas * 16 <= sms && attn_cluster_ok(D, 16)) g.dsplit = 2;
   return g;
 }
 
@@ -246,6 +252,7 @@ cpa_status attn_impl(const cpa_attn_args* a, cudaStream_t stream, bool decode, c
   p.nq = g.nq;
   p.splits = g.splits;
   p.cluster = g.cluster ? 1 : 0;
+  p.dsplit = g.dsplit;
   const double scale = a->scale > 0.f ? static_cast<double>(a->scale) : 1.0 / sqrt(static_cast<double>(a->D));
   p.sl2 = static_cast<float>(scale * 1.4426950408889634);
   p.inv_scale = static_cast<float>(1.0 / scale);

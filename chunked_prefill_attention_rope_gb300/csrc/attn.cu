@@ -17,23 +17,26 @@
 // normalised row and log2-sum-exp straight from tensor memory into the
 // shared memory of the CTA that owns the row's slice (CTA s owns rows
 // [s*128/S, (s+1)*128/S)); after a second cluster barrier each CTA merges its
-// slice from its own shared memory.  Other split counts write the partials
-// to the workspace and combine_kernel merges them.  Both merges take the
-// splits in the same fixed order with the same arithmetic.
+// slice from its own shared memory.  At D = 256 with 8 splits each split is
+// taken by two CTAs (clusters of 16): both compute the same S and P, each
+// forms P V for one half of D, and each half is exchanged and merged among
+// the 8 CTAs that hold it, so a CTA sends half the bytes (the exchange, at
+// ~10 bytes per clock per SM, bounds these calls).  Other split counts write
+// the partials to the workspace and combine_kernel merges them.  Both merges
+// take the splits in the same fixed order with the same arithmetic.
 //
-// Chunk keys: rope_chunk_k_kernel rotates them once per call into the
-// workspace (the append's arithmetic).  The attention grid is launched as a
-// programmatic dependent of it, so its prologue and the Q copy and rotation
-// run while the keys are rotated; it then waits for that grid before it plans
-// from the lengths or reads any cached row.
+// Queries and chunk keys: rope_chunk_k_kernel rotates them once per call into
+// the workspace (the append's arithmetic).  The attention grid is launched as
+// a programmatic dependent of it, so its prologue (barriers, tensor memory)
+// runs while the rows are rotated; it then waits for that grid before it reads
+// anything of the call: the rotated Q tile, the lengths, any cached row.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: K and V tiles into a 2-stage shared-memory ring.
 //   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM S buffers,
 //               O += P V into the TMEM O accumulator; owns the TMEM allocation.
 //   warps 2..5  softmax warpgroup: thread = TMEM lane = packed query row.
-//               Rotates the TMA-loaded Q rows in shared memory at the start,
-//               applies the mask, keeps the running
+//               Applies the mask, keeps the running
 //               max / sum in fp32 (log2 domain, rescaling O only when the max
 //               grows by more than 2^8), writes P as bf16 (fp16 for an fp16
 //               KV cache), and finally scales O by 1/l: into a shared-memory
@@ -106,8 +109,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int qt = blockIdx.x / p.splits;
+  // CTAs of a query tile: p.splits key splits, each taken by p.dsplit CTAs
+  // that divide D for the P V products and the merge (cluster rank
+  // dh * p.splits + split)
+  const int per_q = p.splits * p.dsplit;
+  const int qt = blockIdx.x / per_q;
+  const int dh = (blockIdx.x % per_q) / p.splits;
   const int split = blockIdx.x % p.splits;
+  const int DV = D / p.dsplit;  // value columns of this CTA: [dh * DV, dh * DV + DV)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
 
@@ -194,10 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int blk = 0; blk < D / 64; ++blk)
           tma_load_4d(sK + st * SM::kKBytes + blk * BN * 128, mk, &bars->k_full[st], blk * 64, base, kvh, b);
-        mbar_arrive_expect_tx(&bars->v_full[st], SM::kVBytes);
-#pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(sV + st * SM::kVBytes + blk * BN * 128, mv, &bars->v_full[st], blk * 64, base, kvh, b);
+        mbar_arrive_expect_tx(&bars->v_full[st], static_cast<uint32_t>(SM::kVBytes / p.dsplit));
+        for (int blk = 0; blk < DV / 64; ++blk)
+          tma_load_4d(sV + st * SM::kVBytes + blk * BN * 128, mv, &bars->v_full[st], dh * DV + blk * 64, base, kvh,
+                      b);
         issued = q + 1;
       }
       // Before leaving, make sure no copy is still landing in shared memory.
@@ -215,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const bool leader = elect_lane();
       constexpr uint32_t idesc_qk = idesc_16(kBM, BN, false, F16);
-      constexpr uint32_t idesc_pv = idesc_16(kBM, D, true, F16);
+      constexpr uint32_t idesc_pv_d = idesc_16(kBM, D, true, F16);
+      constexpr uint32_t idesc_pv_h = idesc_16(kBM, D / 2, true, F16);
+      const uint32_t idesc_pv = p.dsplit == 2 ? idesc_pv_h : idesc_pv_d;  // N = DV
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t p_addr = smem_u32(sP);
       bool ok = my_nt > 0 ? warp_all(mbar_wait(&bars->q_full, 0, abort)) : true;
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             uint32_t o32[32];
             const uint32_t ta = tmem + lane_base + SM::kOCol + 32 * c;
             tmem_ld32(ta, o32);
@@ -516,10 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int owner = row / rows_per, slot = row % rows_per;
       named_bar_sync(1, 128);
       asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-      const uint32_t dst = dsmem_addr(smem_u32(smem), owner);
+      const uint32_t dst = dsmem_addr(smem_u32(smem), dh * S + owner);
       dsmem_st(dst + SM::kRecvLse + 4u * (split * rows_per + slot), lse_me);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t o32[32];
         if (my_nt > 0) {
           tmem_ld32(tmem + lane_base + SM::kOCol + 32 * c, o32);
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.y = empty ? 0.f : __uint_as_float(o32[4 * q4 + 1]) * inv_l;
           v.z = empty ? 0.f : __uint_as_float(o32[4 * q4 + 2]) * inv_l;
           v.w = empty ? 0.f : __uint_as_float(o32[4 * q4 + 3]) * inv_l;
-          const uint32_t off = 16u * ((split * (D / 4) + e) * rows_per + (slot ^ (e & 7)));
+          const uint32_t off = 16u * ((split * (DV / 4) + e) * rows_per + (slot ^ (e & 7)));
           dsmem_st4(dst + off, v);
         }
       }
@@ -558,8 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int* tab_i = reinterpret_cast<const int*>(smem + SM::kTabI);
       const int* tab_bh = reinterpret_cast<const int*>(smem + SM::kTabBh);
       const float* rlse = reinterpret_cast<const float*>(smem + SM::kRecvLse);
-      constexpr int NCH = D / 4;                      // float4 chunks per row
-      constexpr int CPL = NCH >= 32 ? NCH / 32 : 1;   // chunks per lane
+      const int nch = DV / 4;                         // float4 chunks of this CTA's columns
+      constexpr int CPL = D / 4 >= 32 ? D / 128 : 1;  // chunks per lane (at most)
+      const int dcol = dh * DV;
       for (int j = w; j < rows_per; j += 4) {
         const int r = split * rows_per + j;
         const long long orow = tab_row[r];
@@ -580,15 +592,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < CPL; ++q) {
             const int e = lane + 32 * q;
-            part[s2][q] = (s2 < S && lane < NCH)
-                              ? *reinterpret_cast<const float4*>(smem + 16u * ((s2 * NCH + e) * rows_per + (j ^ (e & 7))))
+            part[s2][q] = (s2 < S && e < nch)
+                              ? *reinterpret_cast<const float4*>(smem + 16u * ((s2 * nch + e) * rows_per + (j ^ (e & 7))))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
           }
         float4 acc[CPL];
 #pragma unroll
         for (int q = 0; q < CPL; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         float wsum = 0.f;
-        if (lmax != -INFINITY && lane < NCH) {
+        if (lmax != -INFINITY && lane < nch) {
 #pragma unroll
           for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
             if (s2 >= S || ls[s2] == -INFINITY) continue;
@@ -603,17 +615,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (lane >= NCH) continue;
+        if (lane >= nch) continue;
         if (!in_bounds(orow * D, D, n_qo(p), p.err)) continue;
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         const bool is_sel = p.out_sel && tab_i[r] == sel && in_bounds(static_cast<long long>(tab_bh[r]) * D, D, n_sel(p), p.err);
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
           const int e = lane + 32 * q;
+          if (e >= nch) break;
           const float4 o = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
-          *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(orow) * D + 4 * e) =
+          *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(orow) * D + dcol + 4 * e) =
               make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
-          if (is_sel) *reinterpret_cast<float4*>(p.out_sel + static_cast<size_t>(tab_bh[r]) * D + 4 * e) = o;
+          if (is_sel) *reinterpret_cast<float4*>(p.out_sel + static_cast<size_t>(tab_bh[r]) * D + dcol + 4 * e) = o;
         }
       }
     }
@@ -784,8 +797,9 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   using SM = AttnSmem<D, BN>;
   auto kern = attn_kernel<D, BN, F16>;
   static SmemAttr smem_attr;
-  if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), SM::kAlloc); e != cudaSuccess) return e;
-  dim3 grid(p.nq * p.splits, p.Hkv, p.B);
+  if (cudaError_t e = smem_attr.ensure(reinterpret_cast<const void*>(kern), SM::kAlloc, true); e != cudaSuccess)
+    return e;
+  dim3 grid(p.nq * p.splits * p.dsplit, p.Hkv, p.B);
   const long long items = static_cast<long long>(p.B) * (p.Hkv + p.Hq) * p.C * (D / 16);
   const int kblocks = static_cast<int>(max(1LL, min(static_cast<long long>(152) * 8, (items + 255) / 256)));
   cudaError_t e = launch_dependent(rope_chunk_k_kernel, dim3(kblocks), dim3(256), 0, stream, p);
@@ -801,7 +815,7 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   int n = 1;
   if (p.cluster) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = p.splits;
+    attr[1].val.clusterDim.x = p.splits * p.dsplit;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     n = 2;
@@ -811,23 +825,25 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
-// Whether clusters of `splits` CTAs of attn_kernel<D, BN> fit on the device
-// (the fp16 instantiation has the same resources).
+// Whether clusters of `size` CTAs of attn_kernel<D, BN> fit on the device
+// (the fp16 instantiation has the same resources; above 8 a cluster size is
+// non-portable and must be allowed first).
 template <int D, int BN>
-static bool cluster_fits(int splits) {
+static bool cluster_fits(int size) {
   using SM = AttnSmem<D, BN>;
   auto kern = attn_kernel<D, BN, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc) != cudaSuccess) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits);
+  cfg.gridDim = dim3(size);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = SM::kAlloc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = splits;
+  attr[0].val.clusterDim.x = size;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -853,24 +869,24 @@ cudaError_t launch_fused_append_len(const AttnParams& p, cudaStream_t stream) {
   return launch_dependent(fused_len_kernel, dim3(1), dim3(256), 0, stream, p);
 }
 
-bool attn_cluster_ok(int D, int splits) {
-  if (splits < 2 || splits > kMaxClusterSplits) return false;
+bool attn_cluster_ok(int D, int size) {
+  if (size < 2 || size > kMaxClusterSize) return false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  // per device, head dim and split count: 0 unknown, 1 fits, 2 does not
-  static signed char known[16][3][kMaxClusterSplits + 1] = {};
+  // per device, head dim and cluster size: 0 unknown, 1 fits, 2 does not
+  static signed char known[16][3][kMaxClusterSize + 1] = {};
   const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
   if (dev < 0 || dev >= 16) return false;
-  signed char& k = known[dev][di][splits];
+  signed char& k = known[dev][di][size];
   if (k == 0) {
     bool fits = false;
     switch (D) {
-      case 64: fits = cluster_fits<64, 128>(splits); break;
-      case 128: fits = cluster_fits<128, 128>(splits); break;
-      case 256: fits = cluster_fits<256, 64>(splits); break;
+      case 64: fits = cluster_fits<64, 128>(size); break;
+      case 128: fits = cluster_fits<128, 128>(size); break;
+      case 256: fits = cluster_fits<256, 64>(size); break;
       default: break;
     }
     k = fits ? 1 : 2;

@@ -18,13 +18,15 @@ namespace cpa {
 // harmless.
 struct SmemAttr {
   std::atomic<uint64_t> done{0};
-  cudaError_t ensure(const void* kern, int bytes) {
+  cudaError_t ensure(const void* kern, int bytes, bool nonportable_cluster = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && nonportable_cluster)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
     return e;
   }
@@ -95,6 +97,8 @@ struct AttnParams {
   uint16_t* v_cvt;        // fp16 KV cache: the chunk values in fp16 (workspace)
   int cluster;            // single-tile path: the splits of a query tile form one
                           // thread-block cluster and merge their partials in-kernel
+  int dsplit;             // single-tile cluster: 1, or 2 when each split is taken by a
+                          // CTA pair that divides D between them for P V and the merge
   // Fused global append (app_n non-null): the rotated chunk keys and the
   // values of rows [0, n_b) go to cache slots [len_b, len_b + n_b) from the
   // RoPE pre-pass; len is advanced after the attention has read it.
@@ -161,9 +165,10 @@ int attn_block_n(int D);
 // Largest split count whose partials the single-tile kernel merges inside a
 // thread-block cluster (portable cluster size).
 constexpr int kMaxClusterSplits = 8;
+constexpr int kMaxClusterSize = 16;  // CTAs: splits x dsplit
 // True when clusters of `splits` single-tile CTAs of head dim D can run on the
 // current device (checked once per device and size).
-bool attn_cluster_ok(int D, int splits);
+bool attn_cluster_ok(int D, int cluster_size);
 // True when the two-query-tile kernel (256 packed rows per CTA) serves these sizes.
 inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >= 2; }
 // True when the warp-MMA decode kernel (64-key tiles, G <= 16 rows) serves these sizes.
