@@ -51,9 +51,9 @@ KERNEL_SOURCES = {
 }
 MEASURED_TRAFFIC = {
     # long-context chunk call: prep + attn_pair + merge, one ncu capture of the second call
-    "prefill": {"src": "32b96a9ed133f3e3", "bytes": 645291520},
-    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0071 x)
-    "decode": {"src": "960cdf5e090c4d75", "bytes": 4830099533},
+    "prefill": {"src": "dd79b8077f881f86", "bytes": 645589504},
+    # decode call at B = 64, scaled from the B = 16 capture by algorithmic bytes (1.0067 x)
+    "decode": {"src": "f41e512c7c0d7542", "bytes": 4828270940},
 }
 
 def source_hash(kind):

@@ -122,8 +122,10 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0
               attn_cluster_ok(D, g.splits);
   // D = 256 over 8 splits: the merge's exchange of 128 KB of fp32 rows per CTA
   // through distributed shared memory bounds the call, so each split is taken
-  // by two CTAs that divide D (each sends half), in clusters of 16
-  if (g.cluster && g.splits == 8 && D == 256 && ctas * 16 <= sms && attn_cluster_ok(D, 16)) g.dsplit = 2;
+  // by two CTAs that divide D (each sends half), in clusters of 16, when all of
+  // those clusters can be resident at once (not every GPC holds 16 CTAs, and
+  // a second wave of them costs more than the exchange saves)
+  if (g.cluster && g.splits == 8 && D == 256 && ctas * 16 <= sms && ctas <= attn_max_clusters(D, 16)) g.dsplit = 2;
   return g;
 }
 

@@ -825,17 +825,17 @@ static cudaError_t launch_attn_t(const CUtensorMap* maps, const AttnParams& p, c
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
-// Whether clusters of `size` CTAs of attn_kernel<D, BN> fit on the device
-// (the fp16 instantiation has the same resources; above 8 a cluster size is
-// non-portable and must be allowed first).
+// How many clusters of `size` CTAs of attn_kernel<D, BN> can be resident at
+// once (the fp16 instantiation has the same resources; above 8 a cluster size
+// is non-portable and must be allowed first); 0 when none fits.
 template <int D, int BN>
-static bool cluster_fits(int size) {
+static int cluster_count(int size) {
   using SM = AttnSmem<D, BN>;
   auto kern = attn_kernel<D, BN, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(size);
@@ -851,9 +851,9 @@ static bool cluster_fits(int size) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
-  return n > 0;
+  return n > 0 ? n : 0;
 }
 
 static cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
@@ -869,30 +869,39 @@ cudaError_t launch_fused_append_len(const AttnParams& p, cudaStream_t stream) {
   return launch_dependent(fused_len_kernel, dim3(1), dim3(256), 0, stream, p);
 }
 
-bool attn_cluster_ok(int D, int size) {
-  if (size < 2 || size > kMaxClusterSize) return false;
+int attn_max_clusters(int D, int size) {
+  if (size < 2 || size > kMaxClusterSize) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
-  // per device, head dim and cluster size: 0 unknown, 1 fits, 2 does not
-  static signed char known[16][3][kMaxClusterSize + 1] = {};
+  // per device, head dim and cluster size: -1 unknown, else the count
+  static int known[16][3][kMaxClusterSize + 1];
+  static bool init = [] {
+    for (auto& a : known)
+      for (auto& b2 : a)
+        for (int& k : b2) k = -1;
+    return true;
+  }();
+  (void)init;
   const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
-  if (dev < 0 || dev >= 16) return false;
-  signed char& k = known[dev][di][size];
-  if (k == 0) {
-    bool fits = false;
+  if (dev < 0 || dev >= 16) return 0;
+  int& k = known[dev][di][size];
+  if (k < 0) {
+    int n = 0;
     switch (D) {
-      case 64: fits = cluster_fits<64, 128>(size); break;
-      case 128: fits = cluster_fits<128, 128>(size); break;
-      case 256: fits = cluster_fits<256, 64>(size); break;
+      case 64: n = cluster_count<64, 128>(size); break;
+      case 128: n = cluster_count<128, 128>(size); break;
+      case 256: n = cluster_count<256, 64>(size); break;
       default: break;
     }
-    k = fits ? 1 : 2;
+    k = n;
   }
-  return k == 1;
+  return k;
 }
+
+bool attn_cluster_ok(int D, int size) { return attn_max_clusters(D, size) > 0; }
 
 cudaError_t launch_attn(const CUtensorMap* maps, const AttnParams& p, cudaStream_t stream) {
   cudaError_t e;

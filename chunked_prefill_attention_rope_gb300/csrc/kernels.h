@@ -169,6 +169,8 @@ constexpr int kMaxClusterSize = 16;  // CTAs: splits x dsplit
 // True when clusters of `splits` single-tile CTAs of head dim D can run on the
 // current device (checked once per device and size).
 bool attn_cluster_ok(int D, int cluster_size);
+// Clusters of that size that can be resident at once (0: none fits).
+int attn_max_clusters(int D, int cluster_size);
 // True when the two-query-tile kernel (256 packed rows per CTA) serves these sizes.
 inline bool attn_uses_pair(int D, int nq) { return (D == 64 || D == 128) && nq >= 2; }
 // True when the warp-MMA decode kernel (64-key tiles, G <= 16 rows) serves these sizes.
