@@ -41,6 +41,9 @@ CASES = [
     # the plan deals whole blocks to the teams (the planned-order walk)
     small("h_whole_deal_d64", 64, 16, 4, 64, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64)),
     small("h_whole_deal_d128", 48, 16, 4, 128, 64, 384, ("uniform", 128, 384), ("uniform", 1, 64)),
+    # the page-1 call shape: two query tiles of 8 splits, each split taken by
+    # two CTAs that divide D (clusters of 16)
+    small("h_page1_d256", 1, 4, 1, 256, 64, 800, ("fixed", 800), ("fixed", 52)),
 ]
 
 
@@ -134,7 +137,7 @@ def test_f16_sliding_padded_tail_equals_exact_append(prefix, tail):
     assert np.array_equal(bits16(cache.v)[:, :, :Lf], ov_[:, :, :Lf])
 
 
-@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[5], CASES[-1]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[5], CASES[-2], CASES[-1]], ids=lambda w: w.name)
 def test_f16_fused_append_equals_attention_then_append(w):
     cpa = lib()
     inp = {k: v.to(DEV) for k, v in make_chunk_inputs(w).items()}
