@@ -130,7 +130,8 @@ Geometry geometry(int B, int Hq, int Hkv, int D, int C, int P, int sm_budget = 0
 }
 
 // Workspace of the decode and single-tile paths: split-KV partials (when
-// combine_kernel merges them), then the rotated chunk keys (single-tile path).
+// combine_kernel merges them), then, on the single-tile path, the rotated
+// queries and chunk keys and (fp16 cache) the converted chunk values.
 struct SingleWorkspace {
   size_t part_o, part_lse, q_rot, k_rot, v_cvt, total;
 };

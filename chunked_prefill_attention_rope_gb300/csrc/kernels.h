@@ -166,8 +166,8 @@ int attn_block_n(int D);
 // thread-block cluster (portable cluster size).
 constexpr int kMaxClusterSplits = 8;
 constexpr int kMaxClusterSize = 16;  // CTAs: splits x dsplit
-// True when clusters of `splits` single-tile CTAs of head dim D can run on the
-// current device (checked once per device and size).
+// True when clusters of `cluster_size` single-tile CTAs of head dim D can run
+// on the current device (checked once per device and size).
 bool attn_cluster_ok(int D, int cluster_size);
 // Clusters of that size that can be resident at once (0: none fits).
 int attn_max_clusters(int D, int cluster_size);

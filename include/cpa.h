@@ -196,7 +196,8 @@ cpa_status cpa_chunk_prefill_attn(const cpa_attn_args* args, cpa_stream stream);
 cpa_status cpa_decode_step(const cpa_attn_args* args, cpa_stream stream);
 
 /* Bytes of workspace cpa_chunk_prefill_attn / cpa_decode_step need for these
- * sizes (0 when the step runs without split-KV partials). */
+ * sizes: the plan, split-KV partials and rotated copies described under
+ * `workspace` above (0 only for a one-token step that needs no partials). */
 size_t cpa_attn_workspace_size(int B, int Hq, int Hkv, int D, int C, int P);
 
 /* Bytes of workspace for a call with an explicit mask at these sizes: at
@@ -218,9 +219,9 @@ size_t cpa_attn_workspace_size_mask(int B, int Hq, int Hkv, int D, int C, int P)
  * device memory is planned once from static shapes, and plugins inside a host
  * framework that owns the allocator.  Arguments and results are those of
  * cpa_chunk_prefill_attn; args->workspace and args->workspace_bytes are
- * ignored.  Split-KV partials go to one 16 MiB array compiled into the library
- * (held on every GPU that loads the library until the process exits); the
- * call itself allocates nothing.
+ * ignored.  The call's workspace (what cpa_attn_workspace_size counts) is one
+ * 16 MiB array compiled into the library (held on every GPU that loads the
+ * library until the process exits); the call itself allocates nothing.
  *   - Returns CPA_ERR_WORKSPACE, launching nothing, when the sizes need more
  *     than 16 MiB (cpa_attn_workspace_size(...) > 16 MiB).
  *   - The first call on a device looks up the array's device address (with
